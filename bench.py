@@ -1,0 +1,493 @@
+#!/usr/bin/env python
+"""Benchmark of the fused 3x3(x3) convolution hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--path auto|tc|fma] [--no-others]
+
+One step = one conv3d_fused call (valid 3x3x3 conv with the fused epilogue) over
+one batch of seeded synthetic input already resident in HBM.  The default
+workload is conv3d + tanh(mish) on x[16,32,32,64,64] -> [16,64,30,62,62].
+Prints ONE JSON line on rank 0.  Under torchrun each rank runs its own batch
+shard on its own GPU (weak scaling; the only collectives are the timing
+barrier and the max over ranks).
+
+--impl reference times the float64 CPU oracle (the checker) on the host cores,
+each step a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import seeded_inputs as si  # noqa: E402
+
+METRIC = "conv GFLOP/s (2·MACs/time), µs/call, % of fp32/TF32 or HBM roofline"
+UNIT = "GFLOP/s"
+L2_BYTES = 129 * 1024 * 1024
+# Nominal dense tensor rates (PFLOP/s): TF32 / BF16 ratio used to derive the TF32 peak
+# from the measured BF16 GEMM rate.
+TF32_OVER_BF16 = 1.1 / 2.25
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                  "sm_max_mhz": 2070.0}
+SMS = 152
+FMA_PER_SM_PER_CLK = 128
+
+WORKLOADS = {
+    "conv3d_tanh_mish": si.conv3d_tanh_mish,
+    "conv3d_pool_reduce": si.conv3d_pool_reduce,
+    "dwsep": si.dwsep_conv2d,
+    "sweep16": lambda: si.conv3d_sweep(16),
+    "sweep64": lambda: si.conv3d_sweep(64),
+    "sweep128": lambda: si.conv3d_sweep(128),
+    "tiny": si.tiny_conv3d,
+}
+
+
+# ------------------------------------------------------------------ workload arithmetic
+def macs(wl) -> int:
+    d = wl.dims
+    if wl.op == "conv3d":
+        return d["N"] * d["Cout"] * (d["D"] - 2) * (d["H"] - 2) * (d["W"] - 2) * d["Cin"] * 27
+    return d["N"] * d["H"] * d["W"] * d["C"] * (9 + d["Cout"])
+
+
+def compulsory_bytes(wl) -> tuple:
+    """(bytes read, bytes written) if every input is read once and every output written once."""
+    rd = sum(t.numel for t in wl.tensors) * 4
+    d = wl.dims
+    if wl.op == "conv3d":
+        if wl.epilogue == "pool_reduce":
+            wr = d["N"] * 4
+        else:
+            wr = d["N"] * d["Cout"] * (d["D"] - 2) * (d["H"] - 2) * (d["W"] - 2) * 4
+    else:
+        wr = d["N"] * d["Cout"] * d["H"] * d["W"] * 4
+    return rd, wr
+
+
+def describe(wl) -> str:
+    d = wl.dims
+    if wl.op == "conv3d":
+        epi = {"tanh_mish": "tanh(mish)", "pool_reduce": "/2-maxpool2-mean-+bias2-sum_c",
+               "none": "none"}[wl.epilogue]
+        return (f"conv3d k3 valid s1 x[{d['N']},{d['Cin']},{d['D']},{d['H']},{d['W']}] "
+                f"w[{d['Cout']},{d['Cin']},3,3,3] epilogue {epi}")
+    return (f"dwsep conv2d x[{d['N']},{d['C']},{d['H']},{d['W']}] dw 3x3 pad1 -> pw "
+            f"{d['C']}->{d['Cout']}, no bias")
+
+
+def load_peaks() -> tuple:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def roofline_peak(path: str, op: str, peaks: dict, src: str) -> dict:
+    """The roofline the dominant kernel of a path is held to."""
+    if path == "tc" and op == "conv3d":
+        tf32 = peaks["bf16_tflops"] * TF32_OVER_BF16
+        return {"bound": "tensor", "peak": tf32 / 3.0, "unit": "TFLOP/s",
+                "peak_note": (f"3xTF32: dense TF32 peak / 3; TF32 = {src} BF16 GEMM burst "
+                              f"{peaks['bf16_tflops']:.0f} TFLOP/s x nominal TF32/BF16 ratio 1.1/2.25")}
+    if path == "tc":
+        return {"bound": "hbm", "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "peak_note": f"{src} HBM copy bandwidth"}
+    mhz = peaks.get("sm_max_mhz", 2070.0)
+    fma_tf = SMS * FMA_PER_SM_PER_CLK * 2 * mhz * 1e6 / 1e12
+    return {"bound": "alu", "peak": fma_tf, "unit": "TFLOP/s",
+            "peak_note": f"FP32 FMA: {SMS} SMs x {FMA_PER_SM_PER_CLK} FMA/clk x 2 FLOP x {mhz:.0f} MHz"}
+
+
+def traffic_for(kernel_key: str, wl_name: str):
+    """ncu DRAM bytes per launch recorded under profiles/, if the kernel is unchanged since."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f).get(kernel_key, {}).get(wl_name)
+    except (OSError, ValueError):
+        return None
+    if not rec:
+        return None
+    src = os.path.join(ROOT, rec["source"])
+    try:
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    return rec["dram_bytes_per_launch"] if h == rec.get("source_sha256") else None
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, index: int):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [s.strip() for s in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        rows = [r for t, r in self.samples if t0 <= t <= t1 + 0.15]
+        if not rows:
+            rows = [r for _, r in self.samples[-3:]]
+        mhz, mx, reasons = [], [], set()
+        for r in rows:
+            try:
+                mhz.append(float(r[0]))
+                mx.append(float(r[1]))
+            except (ValueError, IndexError):
+                continue
+            for name, v in zip(self.NAMES, r[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not mhz:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(mhz)}
+
+
+# ------------------------------------------------------------------ our arm
+def shard_inputs(wl, rank: int, world: int) -> dict:
+    """Inputs of this rank: batch items [rank*N, (rank+1)*N) of a global batch of N*world."""
+    out = {}
+    x = wl.spec("x")
+    shard_numel = x.numel
+    global_x = x.numel * world
+    off = 0
+    for t in wl.tensors:
+        if t.name == "x":
+            out["x"] = si.draw(wl.seed, rank * shard_numel, t.shape, t.dist)
+            off = global_x
+        else:
+            out[t.name] = si.draw(wl.seed, off, t.shape, t.dist)
+            off += t.numel
+    return out
+
+
+def make_call(ig3, wl, dev_t: dict, path: str):
+    import torch
+    if wl.op == "conv3d":
+        d = wl.dims
+        params = None
+        if wl.epilogue == "pool_reduce":
+            params = {"divisor": wl.divisor, "pool": wl.pool, "bias2": dev_t["bias2"]}
+            out = torch.empty((d["N"],), device=dev_t["x"].device)
+        else:
+            out = torch.empty((d["N"], d["Cout"], d["D"] - 2, d["H"] - 2, d["W"] - 2), device=dev_t["x"].device)
+        need = ig3.conv3d_fused_workspace_size(d["N"], d["Cin"], d["D"], d["H"], d["W"], d["Cout"],
+                                               wl.epilogue, path)
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev_t["x"].device)
+        chosen = ig3.conv3d_fused_select_path(d["N"], d["Cin"], d["D"], d["H"], d["W"], d["Cout"], wl.epilogue,
+                                              path)
+
+        def call():
+            ig3.conv3d_fused(dev_t["x"], dev_t["w"], dev_t.get("b"), epilogue=wl.epilogue, params=params, out=out,
+                             workspace=ws, path=path)
+        return call, out, chosen
+    d = wl.dims
+    out = torch.empty((d["N"], d["Cout"], d["H"], d["W"]), device=dev_t["x"].device)
+    chosen = ig3.dwsep_conv2d_select_path(d["N"], d["C"], d["H"], d["W"], d["Cout"], path)
+
+    def call():
+        ig3.dwsep_conv2d(dev_t["x"], dev_t["w_dw"], dev_t["w_pw"], dev_t.get("b"), out=out, path=path)
+    return call, out, chosen
+
+
+def time_steps(call, steps: int, warmup: int, dist_on: bool):
+    import torch
+    import torch.distributed as dist
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    if dist_on:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    start.record()
+    for _ in range(steps):
+        call()
+    end.record()
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if dist_on:
+        dist.barrier()
+    ms = start.elapsed_time(end)
+    if dist_on:
+        v = torch.tensor([ms], device="cuda", dtype=torch.float64)
+        dist.all_reduce(v, op=dist.ReduceOp.MAX)
+        ms = float(v.item())
+    return ms, t0, t1
+
+
+def e2e_steps(ig3, wl, call, dev_t: dict, out, steps: int, warmup: int):
+    """Same call, with each step's inputs copied from pinned host memory and its output read back."""
+    import torch
+    host = {k: v.cpu().pin_memory() for k, v in dev_t.items()}
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+
+    def step():
+        for k, v in host.items():
+            dev_t[k].copy_(v, non_blocking=True)
+        call()
+        out_host.copy_(out, non_blocking=True)
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        step()
+    end.record()
+    torch.cuda.synchronize()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    return start.elapsed_time(end), h2d, d2h
+
+
+def measure_workload(ig3, wl, path, steps, warmup, peaks, src, rank=0, world=1, dist_on=False, clocks=None):
+    import torch
+    t = shard_inputs(wl, rank, world)
+    dev_t = {k: torch.from_numpy(v).cuda() for k, v in t.items()}
+    call, out, chosen = make_call(ig3, wl, dev_t, path)
+    launches0 = ig3.ig3_kernel_launches()
+    ms, t0, t1 = time_steps(call, steps, warmup, dist_on)
+    launches = ig3.ig3_kernel_launches() - launches0
+    if ig3.ig3_last_device_status() != 0:
+        raise RuntimeError("a kernel reported a device-side timeout during the benchmark")
+    per_step_launches = launches // (steps + warmup) if steps + warmup else 0
+    flop = 2.0 * macs(wl)
+    us = ms * 1e3 / steps
+    gflops = flop * world / (us * 1e-6) / 1e9
+    roof = roofline_peak(chosen, wl.op, peaks, src)
+    if roof["unit"] == "GB/s":
+        rd, wr = compulsory_bytes(wl)
+        achieved = (rd + wr) / (us * 1e-6) / 1e9
+    else:
+        achieved = flop / (us * 1e-6) / 1e12
+    res = {"workload": wl.name, "path": chosen, "us_per_call": us, "gflops": gflops, "ms_total": ms,
+           "timed_launches": per_step_launches * steps, "launches_per_call": per_step_launches,
+           "roofline": {"bound": roof["bound"], "achieved": achieved, "peak": roof["peak"], "unit": roof["unit"],
+                        "frac": achieved / roof["peak"], "peak_note": roof["peak_note"]},
+           "t0": t0, "t1": t1, "dev_t": dev_t, "call": call, "out": out}
+    return res
+
+
+def oracle_sample(wl, target_s: float):
+    """A bounded sample of the workload for the oracle, sized to take about target_s.
+
+    Returns (run, flop, description): run() executes the oracle on the sample and
+    returns its wall time in seconds; flop is the sample's algorithmic FLOP count.
+    """
+    import oracle
+    t = shard_inputs(wl, 0, 1)
+    d = wl.dims
+    if wl.op == "conv3d":
+        def make(planes):
+            xs = np.ascontiguousarray(t["x"][0:1, :, 0:planes + 2])
+
+            def run():
+                t0 = time.perf_counter()
+                y = oracle.conv3d(xs, t["w"], t.get("b"))
+                if wl.epilogue == "tanh_mish":
+                    oracle.tanh_mish(y)
+                elif wl.epilogue == "pool_reduce":
+                    oracle.pool_reduce(y, wl.divisor, wl.pool, t["bias2"])
+                return time.perf_counter() - t0
+            return run, 2.0 * d["Cout"] * planes * (d["H"] - 2) * (d["W"] - 2) * d["Cin"] * 27
+        one, _ = make(2)
+        dt = one()
+        planes = int(max(2, min(d["D"] - 2, 2 * target_s / max(dt, 1e-3))))
+        run, fl = make(planes)
+        return run, fl, f"batch item 0, {planes} of {d['D'] - 2} output planes, all {d['Cout']} channels"
+
+    def make(rows):
+        xs = np.ascontiguousarray(t["x"][0:1, :, 0:rows])
+
+        def run():
+            t0 = time.perf_counter()
+            oracle.dwsep(xs, t["w_dw"], t["w_pw"], t.get("b"))
+            return time.perf_counter() - t0
+        return run, 2.0 * rows * d["W"] * d["C"] * (9 + d["Cout"])
+    one, _ = make(8)
+    dt = one()
+    rows = int(max(8, min(d["H"], 8 * target_s / max(dt, 1e-3))))
+    run, fl = make(rows)
+    return run, fl, f"batch item 0, first {rows} of {d['H']} rows, all {d['Cout']} channels"
+
+
+def cpu_baseline_sample(wl, target_s: float) -> dict:
+    """Time the oracle, as it stands, on a bounded sample of the workload."""
+    import oracle
+    run, fl, sample = oracle_sample(wl, target_s)
+    dt = run()
+    return {"value": fl / dt / 1e9, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": sample, "seconds": dt}
+
+
+def run_ours(args) -> None:
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist_on = world > 1
+    torch.cuda.set_device(local)
+    if dist_on:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import implicit_gemm_convolution_x3x3_gb300 as ig3
+
+    peaks, src = load_peaks()
+    wl = WORKLOADS[args.workload]()
+    sampler = ClockSampler(local) if rank == 0 else None
+    res = measure_workload(ig3, wl, args.path, args.steps, args.warmup, peaks, src, rank, world, dist_on)
+    clocks = sampler.summary(res["t0"], res["t1"]) if sampler else None
+
+    e2e = None
+    if rank == 0:
+        e2e_k = max(3, min(args.steps, 20))
+        ms, h2d, d2h = e2e_steps(ig3, wl, res["call"], res["dev_t"], res["out"], e2e_k, 2)
+        e2e = {"value": 2.0 * macs(wl) / (ms * 1e-3 / e2e_k) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": e2e_k}
+
+    others = []
+    if rank == 0 and not args.no_others and world == 1:
+        for name in ["tiny", "conv3d_pool_reduce", "dwsep", "sweep16", "sweep64", "sweep128"]:
+            if name == args.workload:
+                continue
+            owl = WORKLOADS[name]()
+            k = 200 if name == "tiny" else 10
+            r = measure_workload(ig3, owl, "auto", k, 3, peaks, src)
+            others.append({"workload": name, "desc": describe(owl), "path": r["path"],
+                           "us_per_call": round(r["us_per_call"], 2), "gflops": round(r["gflops"], 1),
+                           "roofline": {k2: (round(v, 4) if isinstance(v, float) else v)
+                                        for k2, v in r["roofline"].items()}})
+            del r
+            torch.cuda.empty_cache()
+    if sampler:
+        sampler.stop()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_sample(wl, target_s=args.cpu_seconds)
+
+    if rank != 0:
+        if dist_on:
+            dist.destroy_process_group()
+        return
+    rd, wr = compulsory_bytes(wl)
+    roof = dict(res["roofline"])
+    kernel_key = "conv3d_tc" if (res["path"] == "tc" and wl.op == "conv3d") else \
+        ("conv3d_fma" if wl.op == "conv3d" else f"dwsep_{res['path']}")
+    roof["traffic"] = traffic_for(kernel_key, wl.name)
+    roof["algorithmic_per_launch"] = (2.0 * macs(wl) / 1e12 if roof["unit"] == "TFLOP/s" else (rd + wr) / 1e9)
+    roof["algorithmic_unit"] = "TFLOP" if roof["unit"] == "TFLOP/s" else "GB"
+    line = {
+        "metric": METRIC, "value": res["gflops"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": res["ms_total"] / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "impl": "ours",
+        "data": "synthetic: seeded SplitMix64 draws, x ~ N(0,1), w and b ~ U(+-1/sqrt(27*Cin))",
+        "config": {"workload": describe(wl), "name": wl.name, "global_batch": wl.dims["N"] * world,
+                   "path": res["path"], "arith": ("3xTF32 on tcgen05 tensor cores, fp32 accumulate"
+                                                  if res["path"] == "tc" else "fp32 FMA"),
+                   "l2": ("inputs larger than L2 (%.0f MB read, %.0f MB written per step; L2 %d MB)"
+                          % (rd / 1e6, wr / 1e6, L2_BYTES // 2**20)),
+                   "parallelism": f"batch shard per GPU x{world}" if world > 1 else "single GPU",
+                   "us_per_call": res["us_per_call"]},
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": res["timed_launches"],
+        "clocks": clocks, "other_workloads": others,
+    }
+    print(json.dumps(line))
+    if dist_on:
+        dist.destroy_process_group()
+
+
+def run_reference(args) -> None:
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    wl = WORKLOADS[args.workload]()
+    # Size each step so the whole --warmup + --steps run stays within about two minutes.
+    per_step = max(0.1, min(2.0, 120.0 / max(1, args.steps + args.warmup)))
+    run, fl, sample = oracle_sample(wl, per_step)
+    for _ in range(args.warmup):
+        run()
+    secs = sum(run() for _ in range(args.steps))
+    value = fl * args.steps / secs / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "impl": "reference",
+        "data": "synthetic: seeded SplitMix64 draws (same inputs as the GPU arm)",
+        "config": {"workload": describe(wl), "name": wl.name, "global_batch": wl.dims["N"],
+                   "arith": "float64 nested loops (the oracle)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"each step: {sample}"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="conv3d_tanh_mish")
+    ap.add_argument("--path", choices=["auto", "tc", "fma"], default="auto")
+    ap.add_argument("--no-others", action="store_true", help="skip the other workloads' summary")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample size in seconds")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

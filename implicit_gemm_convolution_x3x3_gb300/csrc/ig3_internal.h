@@ -1,0 +1,82 @@
+// Host-side internals of the ig3 library: argument bundles, error reporting and
+// the kernel launchers each .cu file provides to the C ABI in ig3_api.cu.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "ig3.h"
+#include "ig3_device.cuh"
+
+namespace ig3 {
+
+struct Conv3dArgs {
+  const float* x;
+  int N, Cin, D, H, W;
+  const float* w;
+  int Cout;
+  const float* b;
+  int epi;
+  float divisor;
+  int pool;
+  const float* bias2;
+  float* y;
+  void* ws;
+  size_t ws_bytes;
+  cudaStream_t stream;
+  int OD() const { return D - 2; }
+  int OH() const { return H - 2; }
+  int OW() const { return W - 2; }
+};
+
+struct DwsepArgs {
+  const float* x;
+  int N, C, H, W;
+  const float* w_dw;
+  const float* w_pw;
+  int Cout;
+  const float* b;
+  float* y;
+  cudaStream_t stream;
+};
+
+// Records a message for ig3_last_error() (thread-local) and returns `status`.
+int fail(int status, const char* fmt, ...);
+// Converts a CUDA error into IG3_ERR_CUDA with a message; IG3_OK for cudaSuccess.
+int cuda_status(cudaError_t e, const char* what);
+// Counts one successful kernel launch (reported by ig3_kernel_launches) and
+// returns `status` unchanged.
+int count_launch(int status);
+// Bounded-wait settings for a launch on the current device.
+WaitCtl wait_ctl();
+// Number of SMs of the current device (cached).
+int num_sms();
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// ---- FMA path (conv3d_fma.cu)
+size_t conv3d_fma_workspace(const Conv3dArgs& a);
+int conv3d_fma_launch(const Conv3dArgs& a);
+
+// ---- tensor-core path (conv3d_tc.cu)
+// Empty string if the TC path handles this shape, else the reason it does not.
+const char* conv3d_tc_unsupported_reason(int N, int Cin, int D, int H, int W, int Cout, int epi);
+size_t conv3d_tc_workspace(const Conv3dArgs& a);
+int conv3d_tc_launch(const Conv3dArgs& a);
+
+// ---- depthwise-separable (dwsep.cu)
+const char* dwsep_tc_unsupported_reason(int N, int C, int H, int W, int Cout);
+int dwsep_fma_launch(const DwsepArgs& a);
+int dwsep_tc_launch(const DwsepArgs& a);
+
+// ---- pool-reduce finalisation shared by both conv3d paths (conv3d_fma.cu):
+// out[n] = scale * sum_{i < per_n} partial[n * per_n + i] + sum_c bias2[c], in a
+// fixed order (deterministic).
+int pool_reduce_finalize(const float* partial, int N, int per_n, float scale, const float* bias2,
+                         int C, float* out, cudaStream_t stream);
+
+// ---- bounded-wait self-test (ig3_api.cu)
+int selftest_bounded_wait(unsigned long long timeout_ns, cudaStream_t stream);
+
+}  // namespace ig3

@@ -1,0 +1,141 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol include/ig3.h
+declares, and rejects bad arguments with status codes before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ig3.h")
+
+
+def _build_if_needed():
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "ig3_build", os.path.join(ROOT, "implicit_gemm_convolution_x3x3_gb300", "build.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod.build()
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = _build_if_needed()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b([a-z_0-9]+)\s*\(", text)) - {"defined"})
+
+
+def test_header_declares_expected_entry_points():
+    names = declared_functions()
+    for n in ("conv3d_fused", "dwsep_conv2d", "ig3_status_string", "ig3_last_device_status",
+              "conv3d_fused_workspace_size"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} is declared in ig3.h but not exported"
+
+
+def test_python_binding_lists_every_symbol():
+    import sys
+    sys.path.insert(0, ROOT)
+    torch = pytest.importorskip("torch")  # noqa: F841  (the binding imports torch)
+    _build_if_needed()
+    import implicit_gemm_convolution_x3x3_gb300 as m
+    assert sorted(m.EXPORTED_SYMBOLS) == declared_functions()
+
+
+def _c(lib):
+    f = lib.conv3d_fused
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p]
+    return f
+
+
+class EpiParams(ctypes.Structure):
+    _fields_ = [("divisor", ctypes.c_float), ("pool", ctypes.c_int), ("bias2", ctypes.c_void_p)]
+
+
+FAKE = 4096  # never dereferenced: every case below fails host-side validation first
+
+
+def test_status_strings(lib):
+    lib.ig3_status_string.restype = ctypes.c_char_p
+    assert lib.ig3_status_string(0) == b"IG3_OK"
+    assert lib.ig3_status_string(-4) == b"IG3_ERR_TIMEOUT"
+    assert lib.ig3_status_string(-5) == b"IG3_ERR_WORKSPACE"
+    assert lib.ig3_status_string(12) == b"IG3_ERR_UNKNOWN"
+
+
+@pytest.mark.parametrize("args,status", [
+    ((1, 1, 3, 3, 3, 1, 0, 0), 0),       # valid (checked below only for the error cases)
+    ((0, 1, 3, 3, 3, 1, 1, 0), -1),      # N = 0
+    ((1, -2, 3, 3, 3, 1, 1, 0), -1),     # Cin < 0
+    ((1, 1, 2, 3, 3, 1, 1, 0), -2),      # D < 3: no valid output
+    ((1, 1, 3, 3, 3, 1, 7, 0), -1),      # unknown epilogue
+    ((1, 1, 3, 3, 3, 1, 1, 9), -1),      # unknown path
+    ((1, 1, 3, 3, 3, 2, 1, 1), -2),      # TC path with Cout = 2
+    ((4096, 64, 64, 64, 64, 64, 1, 0), -1),  # 2^31 or more elements
+    ((1, 1, 3, 3, 3, 1, 2, 0), -2),      # pool-reduce with an empty pooled grid
+])
+def test_conv3d_argument_errors(lib, args, status):
+    f = lib.conv3d_fused_select_path
+    f.restype = ctypes.c_int
+    r = f(*args)
+    if status == 0:
+        assert r in (1, 2)
+    else:
+        assert r == status
+        conv = _c(lib)
+        N, Cin, D, H, W, Cout, epi, path = args
+        assert conv(FAKE, N, Cin, D, H, W, FAKE, Cout, None, epi, None, FAKE, None, 0, path, None) == status
+        lib.ig3_last_error.restype = ctypes.c_char_p
+        assert len(lib.ig3_last_error()) > 0
+
+
+def test_conv3d_null_and_param_errors(lib):
+    conv = _c(lib)
+    assert conv(None, 1, 1, 3, 3, 3, FAKE, 1, None, 1, None, FAKE, None, 0, 2, None) == -1
+    # pool-reduce needs params with bias2, pool == 2 and a finite nonzero divisor
+    assert conv(FAKE, 1, 1, 4, 4, 4, FAKE, 1, None, 2, None, FAKE, None, 0, 2, None) == -1
+    p = EpiParams(2.0, 3, FAKE)
+    assert conv(FAKE, 1, 1, 4, 4, 4, FAKE, 1, None, 2, ctypes.byref(p), FAKE, None, 0, 2, None) == -2
+    p = EpiParams(0.0, 2, FAKE)
+    assert conv(FAKE, 1, 1, 4, 4, 4, FAKE, 1, None, 2, ctypes.byref(p), FAKE, None, 0, 2, None) == -1
+    p = EpiParams(float("inf"), 2, FAKE)
+    assert conv(FAKE, 1, 1, 4, 4, 4, FAKE, 1, None, 2, ctypes.byref(p), FAKE, None, 0, 2, None) == -1
+    # a needed workspace that is missing, too small or misaligned
+    lib.conv3d_fused_workspace_size.restype = ctypes.c_size_t
+    need = lib.conv3d_fused_workspace_size(1, 1, 4, 4, 4, 1, 2, 2)
+    assert need > 0
+    p = EpiParams(2.0, 2, FAKE)
+    assert conv(FAKE, 1, 1, 4, 4, 4, FAKE, 1, None, 2, ctypes.byref(p), FAKE, None, 0, 2, None) == -5
+    assert conv(FAKE, 1, 1, 4, 4, 4, FAKE, 1, None, 2, ctypes.byref(p), FAKE, FAKE, need - 1, 2, None) == -5
+    assert conv(FAKE, 1, 1, 4, 4, 4, FAKE, 1, None, 2, ctypes.byref(p), FAKE, FAKE + 4, need, 2, None) == -5
+
+
+def test_dwsep_argument_errors(lib):
+    f = lib.dwsep_conv2d
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] + [ctypes.c_int] * 4 + [ctypes.c_void_p] * 2 + [ctypes.c_int] + \
+        [ctypes.c_void_p] * 2 + [ctypes.c_int, ctypes.c_void_p]
+    assert f(FAKE, 0, 4, 5, 5, FAKE, FAKE, 4, None, FAKE, 2, None) == -1
+    assert f(FAKE, 1, 4, 5, 5, FAKE, FAKE, 4, None, FAKE, 5, None) == -1
+    assert f(None, 1, 4, 5, 5, FAKE, FAKE, 4, None, FAKE, 2, None) == -1
+    assert f(FAKE, 1, 4, 5, 5, FAKE, FAKE, 4, None, FAKE, 1, None) == -2   # TC: Cout = 4
+    assert f(FAKE, 70000, 64, 512, 512, FAKE, FAKE, 4, None, FAKE, 2, None) == -1  # too many elements
+
+
+def test_workspace_query_is_zero_for_rejected_args(lib):
+    lib.conv3d_fused_workspace_size.restype = ctypes.c_size_t
+    assert lib.conv3d_fused_workspace_size(0, 1, 3, 3, 3, 1, 1, 0) == 0
+    assert lib.conv3d_fused_workspace_size(1, 1, 3, 3, 3, 1, 1, 2) == 0  # tanh-mish on FMA needs none

@@ -1,0 +1,197 @@
+"""GPU parity of conv3d_fused (both paths) against the float64 oracle.
+
+Small cases are compared element by element on every output; the full-size
+workloads (in the launch configuration the benchmark times) are compared on
+sampled outputs the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import seeded_inputs as si
+from parity import assert_close, sample_indices, to_dev
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ig3():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import implicit_gemm_convolution_x3x3_gb300 as m
+    return m
+
+
+def tc_supported(ig3, N, Cin, D, H, W, Cout, epi):
+    try:
+        ig3.conv3d_fused_select_path(N, Cin, D, H, W, Cout, epi, "tc")
+        return True
+    except ig3.Ig3Error:
+        return False
+
+
+def run_conv(ig3, t, epi, path, params=None):
+    x = to_dev(t["x"]); w = to_dev(t["w"])
+    b = to_dev(t["b"]) if "b" in t else None
+    dev_params = None
+    if epi == "pool_reduce":
+        dev_params = dict(params or {})
+        dev_params["bias2"] = to_dev(t["bias2"])
+    out = ig3.conv3d_fused(x, w, b, epilogue=epi, params=dev_params, path=path)
+    assert ig3.ig3_last_device_status() == 0
+    return out.cpu().numpy()
+
+
+def paths_for(ig3, shape, epi):
+    N, Cin, D, H, W, Cout = shape
+    ps = ["fma"]
+    if tc_supported(ig3, N, Cin, D, H, W, Cout, epi):
+        ps.append("tc")
+    return ps
+
+
+# (N, Cin, D, H, W, Cout): several tiles of both kernels and ragged tails in every dim.
+SMALL_CASES = [
+    (2, 32, 6, 20, 70, 64),   # ragged columns and rows for both tilings
+    (1, 8, 5, 11, 64, 16),    # W = 64 (two input rows per 128-position tile)
+    (2, 16, 4, 9, 8, 16),     # narrow rows (W = 8)
+    (1, 16, 4, 6, 64, 128),   # Cout = 128
+    (1, 24, 3, 7, 33, 48),    # Cin not a multiple of 8, Cout = 48
+    (2, 3, 5, 7, 9, 5),       # odd channel counts
+    (1, 1, 3, 3, 3, 1),       # smallest valid input: one output
+]
+
+
+@pytest.mark.parametrize("shape", SMALL_CASES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("epi", ["tanh_mish", "none"])
+def test_conv3d_small_all_outputs(ig3, shape, epi):
+    N, Cin, D, H, W, Cout = shape
+    wl = si.conv3d_workload("t", N, Cin, D, H, W, Cout, seed=1000 + sum(shape), epilogue=epi)
+    t = wl.generate_all()
+    y = oracle.conv3d(t["x"], t["w"], t["b"])
+    ref = oracle.tanh_mish(y) if epi == "tanh_mish" else y
+    for path in paths_for(ig3, shape, epi):
+        got = run_conv(ig3, t, epi, path)
+        assert_close(got, ref, f"{shape} {epi} {path}")
+
+
+def test_tiny_workload_all_outputs(ig3):
+    wl = si.tiny_conv3d()
+    t = wl.generate_all()
+    ref = oracle.conv3d_tanh_mish(t["x"], t["w"], t["b"])
+    for path in paths_for(ig3, tuple(wl.dims.values()), "tanh_mish") + ["auto"]:
+        assert_close(run_conv(ig3, t, "tanh_mish", path), ref, f"tiny {path}")
+
+
+def test_conv3d_without_bias(ig3):
+    wl = si.conv3d_workload("t", 1, 16, 4, 8, 64, 32, seed=77, epilogue="tanh_mish", with_bias=False)
+    t = wl.generate_all()
+    ref = oracle.conv3d_tanh_mish(t["x"], t["w"], None)
+    for path in paths_for(ig3, (1, 16, 4, 8, 64, 32), "tanh_mish"):
+        assert_close(run_conv(ig3, t, "tanh_mish", path), ref, f"no bias {path}")
+
+
+def test_activation_over_wide_range(ig3):
+    # Large weights drive conv outputs across [-60, 60]: exercises both branches
+    # of the activation and its saturation.
+    wl = si.conv3d_workload("t", 1, 8, 4, 6, 64, 16, seed=78, epilogue="tanh_mish", wb_bound=2.5,
+                            x_dist=("uniform", -3.0, 3.0))
+    t = wl.generate_all()
+    y = oracle.conv3d(t["x"], t["w"], t["b"])
+    assert y.min() < -20 and y.max() > 20
+    ref = oracle.tanh_mish(y)
+    for path in paths_for(ig3, (1, 8, 4, 6, 64, 16), "tanh_mish"):
+        assert_close(run_conv(ig3, t, "tanh_mish", path), ref, f"wide range {path}")
+
+
+# ---------------------------------------------------------------- full-size, sampled
+FULL = {
+    "conv3d_tanh_mish": si.conv3d_tanh_mish,
+    "sweep16": lambda: si.conv3d_sweep(16),
+    "sweep64": lambda: si.conv3d_sweep(64),
+    "sweep128": lambda: si.conv3d_sweep(128),
+}
+
+
+@pytest.mark.parametrize("name", list(FULL))
+def test_full_size_sampled(ig3, name):
+    wl = FULL[name]()
+    t = wl.generate_all()
+    d = wl.dims
+    x = to_dev(t["x"]); w = to_dev(t["w"]); b = to_dev(t["b"])
+    out = ig3.conv3d_fused(x, w, b, epilogue="tanh_mish")          # the benchmark's call
+    assert ig3.ig3_last_device_status() == 0
+    idx = sample_indices(tuple(out.shape), 6000, seed=len(name))
+    got = out[tuple(torch.from_numpy(idx.T).to(out.device))].cpu().numpy()
+    ref = oracle.tanh_mish(oracle.conv3d_at(t["x"], t["w"], t["b"], idx))
+    assert_close(got, ref, f"{name} sampled")
+    # Every output is finite and inside the range of tanh.
+    assert bool(torch.isfinite(out).all()) and float(out.abs().max()) <= 1.0
+    del x, w, b, out
+    torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------- pool-reduce
+POOL_CASES = [
+    (3, 8, 6, 10, 64, 16),    # W = 64: two rows per tensor-core tile
+    (2, 8, 6, 8, 8, 16),      # W = 8
+    (2, 4, 7, 9, 13, 16),     # odd conv-output dims: floor mode drops a plane, row, column
+    (1, 5, 4, 4, 4, 3),       # smallest pooled grid (1x1x1), odd channels
+    (2, 16, 5, 12, 32, 32),   # W = 32, odd conv-output depth
+]
+
+
+@pytest.mark.parametrize("shape", POOL_CASES, ids=lambda s: "x".join(map(str, s)))
+def test_pool_reduce_small(ig3, shape):
+    N, Cin, D, H, W, Cout = shape
+    wl = si.conv3d_workload("t", N, Cin, D, H, W, Cout, seed=2000 + sum(shape), epilogue="pool_reduce",
+                            bias2=True)
+    t = wl.generate_all()
+    for div in (2.0, -1.5):
+        ref = oracle.conv3d_pool_reduce(t["x"], t["w"], t["b"], div, 2, t["bias2"])
+        for path in paths_for(ig3, shape, "pool_reduce"):
+            got = run_conv(ig3, t, "pool_reduce", path, params={"divisor": div, "pool": 2})
+            assert_close(got, ref, f"{shape} div={div} {path}")
+
+
+def test_pool_reduce_full_size_sampled_and_deterministic(ig3):
+    wl = si.conv3d_pool_reduce()
+    t = wl.generate_all()
+    x = to_dev(t["x"]); w = to_dev(t["w"]); b = to_dev(t["b"]); bias2 = to_dev(t["bias2"])
+    params = {"divisor": 2.0, "pool": 2, "bias2": bias2}
+    out1 = ig3.conv3d_fused(x, w, b, epilogue="pool_reduce", params=params).cpu().numpy()
+    out2 = ig3.conv3d_fused(x, w, b, epilogue="pool_reduce", params=params).cpu().numpy()
+    assert ig3.ig3_last_device_status() == 0
+    assert out1.shape == (128,)
+    assert np.array_equal(out1, out2), "pool-reduce is not deterministic"
+    for n in (0, 1, 64, 127):
+        ref = oracle.conv3d_pool_reduce(t["x"][n:n + 1], t["w"], t["b"], 2.0, 2, t["bias2"])
+        assert_close(out1[n:n + 1], ref, f"pool-reduce full n={n}")
+
+
+# ---------------------------------------------------------------- edges of the boundary
+def test_output_canaries_untouched(ig3):
+    wl = si.conv3d_workload("t", 1, 8, 5, 9, 64, 16, seed=91, epilogue="tanh_mish")
+    t = wl.generate_all()
+    x = to_dev(t["x"]); w = to_dev(t["w"]); b = to_dev(t["b"])
+    n_out = 1 * 16 * 3 * 7 * 62
+    for path in paths_for(ig3, (1, 8, 5, 9, 64, 16), "tanh_mish"):
+        buf = torch.full((n_out + 2048,), 12345.0, device="cuda")
+        out = buf[1024:1024 + n_out].view(1, 16, 3, 7, 62)
+        ig3.conv3d_fused(x, w, b, epilogue="tanh_mish", out=out, path=path)
+        torch.cuda.synchronize()
+        assert bool((buf[:1024] == 12345.0).all()) and bool((buf[1024 + n_out:] == 12345.0).all()), path
+
+
+def test_errors_are_reported_not_raised_on_device(ig3):
+    x = torch.zeros(1, 2, 3, 3, 3, device="cuda")
+    w = torch.zeros(2, 2, 3, 3, 3, device="cuda")
+    with pytest.raises(ig3.Ig3Error) as e:
+        ig3.conv3d_fused(x, w, None, epilogue="pool_reduce", params={"bias2": torch.zeros(2, device="cuda")})
+    assert e.value.status == -2  # 1x1x1 conv output: the pooled grid is empty
+    with pytest.raises(ig3.Ig3Error) as e:
+        ig3.conv3d_fused(x, w, None, epilogue="tanh_mish", path="tc")
+    assert e.value.status == -2  # Cout = 2 is not a tensor-core shape
+    torch.cuda.synchronize()
+    assert ig3.ig3_last_device_status() == 0
