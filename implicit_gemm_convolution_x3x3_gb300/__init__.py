@@ -24,6 +24,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "l
 __all__ = [
     "EPILOGUES", "PATHS", "Ig3Error", "lib", "conv3d_fused", "dwsep_conv2d",
     "conv3d_fused_workspace_size", "conv3d_fused_select_path", "dwsep_conv2d_select_path",
+    "conv3d_fused_noalloc", "NOALLOC_SCRATCH_BYTES",
     "ig3_status_string", "ig3_last_error", "ig3_last_device_status", "ig3_set_wait_timeout_ns",
     "ig3_selftest_bounded_wait", "ig3_kernel_launches", "ig3_version", "EXPORTED_SYMBOLS",
 ]
@@ -31,6 +32,7 @@ __all__ = [
 EPILOGUES = {"none": 0, "tanh_mish": 1, "pool_reduce": 2}
 PATHS = {"auto": 0, "tc": 1, "fma": 2}
 PATH_NAMES = {1: "tc", 2: "fma"}
+NOALLOC_SCRATCH_BYTES = 4 * 1024 * 1024  # IG3_NOALLOC_SCRATCH_BYTES in include/ig3.h
 STATUS = {0: "IG3_OK", -1: "IG3_ERR_INVALID_ARG", -2: "IG3_ERR_UNSUPPORTED", -3: "IG3_ERR_CUDA",
           -4: "IG3_ERR_TIMEOUT", -5: "IG3_ERR_WORKSPACE"}
 
@@ -53,6 +55,8 @@ _SIGS = {
     "conv3d_fused_workspace_size": (_sz, [_i] * 8),
     "conv3d_fused": (_i, [_p, _i, _i, _i, _i, _i, _p, _i, _p, _i, ctypes.POINTER(_EpiParams), _p, _p, _sz,
                           _i, _p]),
+    "conv3d_fused_noalloc": (_i, [_p, _i, _i, _i, _i, _i, _p, _i, _p, _i, ctypes.POINTER(_EpiParams), _p, _i,
+                                  _p]),
     "dwsep_conv2d": (_i, [_p, _i, _i, _i, _i, _p, _p, _i, _p, _p, _i, _p]),
     "conv3d_fused_select_path": (_i, [_i] * 8),
     "dwsep_conv2d_select_path": (_i, [_i] * 6),
@@ -192,6 +196,46 @@ def conv3d_fused(x: torch.Tensor, w: torch.Tensor, b: torch.Tensor | None = None
         st = lib.conv3d_fused(xp, N, Cin, D, H, W, wp, Cout, bp, epi,
                               None if pr is None else ctypes.byref(pr), yp, wsp, wsb, pth,
                               _stream_handle(stream, x.device))
+    _check(st)
+    return out
+
+
+def conv3d_fused_noalloc(x: torch.Tensor, w: torch.Tensor, b: torch.Tensor | None = None,
+                         epilogue="tanh_mish", params: dict | None = None, out: torch.Tensor | None = None,
+                         path="auto", stream=None) -> torch.Tensor:
+    """conv3d_fused with the scratch taken from the library's static buffer.
+
+    For callers that cannot allocate device memory per call.  ``out`` must be given
+    for the call itself to allocate nothing (else it is created here with torch).
+    See include/ig3.h for the buffer size, the first-call set-up and the rule that
+    calls overlapping on the GPU race on the shared buffer.
+    """
+    epi = _enum(EPILOGUES, epilogue, "epilogue")
+    pth = _enum(PATHS, path, "path")
+    if x.dim() != 5 or w.dim() != 5:
+        raise ValueError("x must be [N,Cin,D,H,W] and w [Cout,Cin,3,3,3]")
+    N, Cin, D, H, W = x.shape
+    Cout = w.shape[0]
+    xp = _dev_f32(x, "x")
+    wp = _dev_f32(w, "w", (Cout, Cin, 3, 3, 3))
+    bp = None if b is None else _dev_f32(b, "b", (Cout,))
+    pr = None
+    if epi == EPILOGUES["pool_reduce"]:
+        params = params or {}
+        if params.get("bias2") is None:
+            raise ValueError("pool_reduce needs params['bias2']")
+        pr = _EpiParams(float(params.get("divisor", 2.0)), int(params.get("pool", 2)),
+                        _dev_f32(params["bias2"], "bias2", (Cout,)))
+        oshape = (N,)
+    else:
+        oshape = (N, Cout, D - 2, H - 2, W - 2)
+    if out is None:
+        out = torch.empty(oshape, dtype=torch.float32, device=x.device)
+    yp = _dev_f32(out, "out", oshape)
+    with torch.cuda.device(x.device):
+        st = lib.conv3d_fused_noalloc(xp, N, Cin, D, H, W, wp, Cout, bp, epi,
+                                      None if pr is None else ctypes.byref(pr), yp, pth,
+                                      _stream_handle(stream, x.device))
     _check(st)
     return out
 

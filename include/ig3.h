@@ -102,6 +102,37 @@ int conv3d_fused(const float* x, int N, int Cin, int D, int H, int W,
                  float* y, void* workspace, size_t workspace_bytes,
                  int path, void* stream);
 
+/* Size of the library's own scratch buffer used by conv3d_fused_noalloc (4 MiB). */
+#define IG3_NOALLOC_SCRATCH_BYTES (4u * 1024u * 1024u)
+
+/*
+ * conv3d_fused without a workspace argument, for callers that cannot allocate
+ * device memory: for instance a host runtime that has reserved the whole device
+ * memory budget and forbids further allocations, a latency-critical path that
+ * cannot afford cudaMalloc's implicit device-wide synchronisation, or code with no
+ * allocator at hand.  The source pages have no counterpart to this entry point; it
+ * is an addition of this library.
+ *
+ * Arguments, layouts, results and error codes are those of conv3d_fused; the
+ * caller still passes (and owns) x, w, b, params->bias2 and y.  The scratch comes
+ * from a static buffer of IG3_NOALLOC_SCRATCH_BYTES inside the library, which every
+ * device that loads the library keeps until the process exits; nothing is
+ * allocated by this call.
+ *   - Shapes whose scratch (conv3d_fused_workspace_size) exceeds the buffer are
+ *     rejected with IG3_ERR_WORKSPACE before anything is launched.
+ *   - The first call on each device looks up the buffer's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one buffer, and it keeps the last call's
+ *     contents.  No part of it needs to start at zero (each call rewrites all it
+ *     reads), but calls whose work overlaps on the GPU (different streams, or
+ *     host threads without ordering between them) race on it: order them.
+ */
+int conv3d_fused_noalloc(const float* x, int N, int Cin, int D, int H, int W,
+                         const float* w, int Cout, const float* b,
+                         int epilogue, const ig3_epi_params* params,
+                         float* y, int path, void* stream);
+
 /*
  * Depthwise-separable conv2d ([P86], the per-output pseudo-code with stride 1,
  * padding 1, dilation 1):
