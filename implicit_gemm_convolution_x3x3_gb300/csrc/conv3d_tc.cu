@@ -24,13 +24,16 @@
 // into 2*Cout accumulator columns (summed in the epilogue) and the third is a
 // second MMA into the first Cout columns; for Cout > 64 three MMAs of N = Cout.
 //
-// Data flow (persistent CTAs, one per SM, 384 threads, warp-specialised):
+// Data flow (persistent CTAs, one per SM, 512 threads, warp-specialised):
 //   warp 0      weight producer: 1-D bulk copies (TMA) of pre-split K-step blocks
-//               [hi rows ; lo rows] from the workspace into a ring of stages, or
-//               all blocks once when they fit (resident weights);
-//   warp 1      TMEM owner and MMA issuer (one thread);
+//               [hi rows ; lo rows] from the workspace into a ring of stages (one
+//               stage = the K-steps of one tap, up to 16 KB), or all blocks once
+//               when they fit (resident weights);
+//   warp 1      TMEM owner and MMA issuer (one thread; descriptors are formed once
+//               and advanced by adds, which keeps issue at the tensor pipe's rate);
 //   warps 2-7   input convert: coalesced loads of x, hi/lo split, K-major stores;
-//   warps 8-11  epilogue: tcgen05.ld, bias, activation or pool-reduce, stores.
+//   warps 8-15  epilogue, two groups of four (one warp per TMEM lane quadrant each):
+//               tcgen05.ld, bias, activation or pool-reduce, stores.
 // A work unit is (batch item n, group of T position tiles, range of output
 // planes).  Input planes stream through a 2-stage A buffer; each input plane d
 // feeds output planes d, d-1, d-2 (kd = 0, 1, 2), whose accumulators live in a
@@ -55,9 +58,10 @@
 namespace ig3 {
 namespace {
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr int kConvWarp0 = 2, kConvThreads = 192;
-constexpr int kEpiWarp0 = 8, kEpiThreads = 128;
+constexpr int kEpiWarp0 = 8, kEpiThreads = 256;  // two warps per TMEM lane quadrant
+constexpr int kStageTarget = 16 * 1024;           // bytes of weights per ring stage
 constexpr int kSlots = 4;
 constexpr int kAStages = 2;
 constexpr int kTmemCols = 512;
@@ -82,6 +86,7 @@ struct TcParams {
   int units;
   int resident;  // weights loaded once
   int SB;        // weight ring stages (streaming)
+  int KSS;       // K-step blocks per ring stage (all of one tap, up to kStageTarget bytes)
   int epi;
   float inv_div;
   uint32_t a_half_bytes;   // one of hi / lo in an A stage
@@ -133,6 +138,12 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __all_sync(0xffffffffu, ok) != 0;
 }
 
+// The common case inline (phase already complete), the bounded loop out of line.
+__device__ __forceinline__ bool wait_fast(uint64_t* bar, uint32_t parity, const WaitCtl& ctl, volatile int* abort) {
+  if (mbar_try_wait(smem_addr(bar), parity)) return true;
+  return mbar_wait_bounded(bar, parity, ctl, abort);
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
@@ -141,12 +152,12 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, float b, fl
   asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
-template <int EPI>
+template <int EPI, int SCHEME>
 __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ float s_red[4];
+  __shared__ float s_red[kEpiThreads / 32];
 
   uint8_t* smem_a = smem;
   uint8_t* smem_b = smem + p.off_b;
@@ -218,13 +229,17 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
                 const int od = d - kd;
                 if (od < un.od0 || od >= un.od1) continue;
                 for (int khw = 0; khw < 9; ++khw) {
-                  for (int ks = 0; ks < ks_n; ++ks) {
-                    if (!mbar_wait_bounded(&b_empty[rb.idx], rb.phase ^ 1u, p.ctl, abort_flag)) goto producer_done;
-                    const int blk = (kd * 9 + khw) * p.KS + ch * (p.CC >> 3) + ks;
-                    mbar_arrive_expect_tx(&b_full[rb.idx], p.b_block_bytes);
-                    bulk_copy_g2s(smem_b + (size_t)rb.idx * p.b_block_bytes,
-                                  reinterpret_cast<const uint8_t*>(p.wblob) + (size_t)blk * p.b_block_bytes,
-                                  p.b_block_bytes, &b_full[rb.idx]);
+                  // One stage = up to KSS consecutive K-step blocks of this tap (contiguous
+                  // in the blob), fetched with one bulk copy.
+                  for (int s0 = 0; s0 < ks_n; s0 += p.KSS) {
+                    const int nb = min(p.KSS, ks_n - s0);
+                    if (!wait_fast(&b_empty[rb.idx], rb.phase ^ 1u, p.ctl, abort_flag)) goto producer_done;
+                    const int blk = (kd * 9 + khw) * p.KS + ch * (p.CC >> 3) + s0;
+                    const uint32_t bytes = (uint32_t)nb * p.b_block_bytes;
+                    mbar_arrive_expect_tx(&b_full[rb.idx], bytes);
+                    bulk_copy_g2s(smem_b + (size_t)rb.idx * p.KSS * p.b_block_bytes,
+                                  reinterpret_cast<const uint8_t*>(p.wblob) + (size_t)blk * p.b_block_bytes, bytes,
+                                  &b_full[rb.idx]);
                     rb.next(p.SB);
                     ++issued;
                   }
@@ -253,12 +268,22 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc_cat = umma_idesc_tf32(128, p.scheme == 0 ? 2 * p.Cout : p.Cout);
+      // Descriptors are formed once and advanced by plain adds in 16-byte units (the
+      // start-address field is the low 14 bits): the issue loop must stay a short
+      // chain of adds for tcgen05.mma to issue at the tensor pipe's rate.
+      const uint32_t idesc_cat = umma_idesc_tf32(128, SCHEME == 0 ? 2 * p.Cout : p.Cout);
       const uint32_t idesc_one = umma_idesc_tf32(128, p.Cout);
-      const uint32_t a_lbo = (uint32_t)p.NPOS * 16u;
-      const uint32_t b_lbo = (uint32_t)(2 * p.Cout) * 16u;
-      const uint32_t a_base = smem_addr(smem_a);
-      const uint32_t b_base = smem_addr(smem_b);
+      const uint64_t a_desc0 = umma_desc_noswizzle(smem_addr(smem_a), (uint32_t)p.NPOS * 16u, 128);
+      const uint64_t b_desc0 = umma_desc_noswizzle(smem_addr(smem_b), (uint32_t)(2 * p.Cout) * 16u, 128);
+      const uint32_t a_stage_u = p.a_stage_bytes >> 4, a_half_u = p.a_half_bytes >> 4;
+      const uint32_t ks_u = 2u * (uint32_t)p.NPOS;       // next K-step: two channel groups on
+      const uint32_t b_block_u = p.b_block_bytes >> 4;
+      const uint32_t b_stage_u = b_block_u * (uint32_t)p.KSS;
+      const uint32_t b_lo_u = (uint32_t)p.Cout;           // lo rows start Cout rows further
+      const uint32_t row_u = (uint32_t)p.W;               // one input row (kh step)
+      const uint32_t slot_cols = (uint32_t)(p.T * p.NACC);
+      const uint32_t nacc = (uint32_t)p.NACC;
+      const int T = p.T, KSS = p.KSS, CC8 = p.CC >> 3;
       bool ok = true;
       if (p.resident) ok = mbar_wait_bounded(w_full, 0, p.ctl, abort_flag);
       Ring ra, rb;
@@ -268,53 +293,65 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
         for (int d = un.od0; ok && d < un.od1 + 2; ++d) {
           for (int ch = 0; ok && ch < p.nchunks; ++ch) {
             const int ks_n = chunk_channels(p, ch) >> 3;
-            if (!(ok = mbar_wait_bounded(&a_full[ra.idx], ra.phase, p.ctl, abort_flag))) break;
+            if (!(ok = wait_fast(&a_full[ra.idx], ra.phase, p.ctl, abort_flag))) break;
             tc_fence_after();
-            const uint32_t a_hi = a_base + ra.idx * p.a_stage_bytes;
-            const uint32_t a_lo = a_hi + p.a_half_bytes;
+            const uint64_t ah0 = a_desc0 + (uint64_t)(ra.idx * a_stage_u);
+            const uint64_t al0 = ah0 + a_half_u;
             for (int kd = 2; ok && kd >= 0; --kd) {
               const int od = d - kd;
               if (od < un.od0 || od >= un.od1) continue;
               const uint32_t pseq = plane_seq + (uint32_t)(od - un.od0);
               const uint32_t slot = pseq & (kSlots - 1);
               if (kd == 0 && ch == 0) {
-                if (!(ok = mbar_wait_bounded(&acc_empty[slot], ((pseq >> 2) & 1u) ^ 1u, p.ctl, abort_flag))) break;
+                if (!(ok = wait_fast(&acc_empty[slot], ((pseq >> 2) & 1u) ^ 1u, p.ctl, abort_flag))) break;
                 tc_fence_after();
               }
-              const uint32_t d_col = tmem_base + slot * (uint32_t)(p.T * p.NACC);
-              for (int khw = 0; ok && khw < 9; ++khw) {
-                const int kh = khw / 3, kw = khw % 3;
-                for (int ks = 0; ks < ks_n; ++ks) {
-                  uint32_t bsm;
-                  if (p.resident) {
-                    bsm = b_base + (uint32_t)(((kd * 9 + khw) * p.KS + ch * (p.CC >> 3) + ks)) * p.b_block_bytes;
-                  } else {
-                    if (!(ok = mbar_wait_bounded(&b_full[rb.idx], rb.phase, p.ctl, abort_flag))) break;
-                    tc_fence_after();
-                    bsm = b_base + rb.idx * p.b_block_bytes;
-                  }
-                  const uint32_t first = (kd == 0 && ch == 0 && khw == 0 && ks == 0) ? 1u : 0u;
-                  const uint64_t b_hi = umma_desc_noswizzle(bsm, b_lbo, 128);
-                  const uint64_t b_lo = umma_desc_noswizzle(bsm + (uint32_t)p.Cout * 16u, b_lbo, 128);
-                  for (int t = 0; t < p.T; ++t) {
-                    const uint32_t a_off = (uint32_t)(t * 128 + kh * p.W + kw) * 16u + (uint32_t)(2 * ks) * a_lbo;
-                    const uint64_t dah = umma_desc_noswizzle(a_hi + a_off, a_lbo, 128);
-                    const uint64_t dal = umma_desc_noswizzle(a_lo + a_off, a_lbo, 128);
-                    const uint32_t dt = d_col + (uint32_t)(t * p.NACC);
-                    if (p.scheme == 0) {
-                      umma_tf32(dt, dah, b_hi, idesc_cat, first ^ 1u);
-                      umma_tf32(dt, dal, b_hi, idesc_one, 1u);
+              const uint32_t d0 = tmem_base + slot * slot_cols;
+              // The first MMA of a plane (kd = 0, first chunk, first tap, first K-step)
+              // overwrites the accumulator; every later one adds to it.
+              uint32_t acc = (kd == 0 && ch == 0) ? 0u : 1u;
+#pragma unroll
+              for (int kh = 0; kh < 3; ++kh) {
+#pragma unroll
+                for (int kw = 0; kw < 3; ++kw) {
+                  const uint32_t tap_u = (uint32_t)kh * row_u + (uint32_t)kw;
+                  const int tap = (kd * 3 + kh) * 3 + kw;
+                  for (int s0 = 0; s0 < ks_n; s0 += KSS) {
+                    const int nb = min(KSS, ks_n - s0);
+                    uint64_t bst;
+                    if (p.resident) {
+                      bst = b_desc0 + (uint64_t)((uint32_t)(tap * p.KS + ch * CC8 + s0) * b_block_u);
                     } else {
-                      umma_tf32(dt, dah, b_hi, idesc_one, first ^ 1u);
-                      umma_tf32(dt, dah, b_lo, idesc_one, 1u);
-                      umma_tf32(dt, dal, b_hi, idesc_one, 1u);
+                      if (!(ok = wait_fast(&b_full[rb.idx], rb.phase, p.ctl, abort_flag))) break;
+                      tc_fence_after();
+                      bst = b_desc0 + (uint64_t)(rb.idx * b_stage_u);
+                    }
+                    for (int j = 0; j < nb; ++j) {
+                      const uint64_t bh = bst + (uint64_t)(j * b_block_u);
+                      const uint64_t koff = (uint64_t)((uint32_t)(s0 + j) * ks_u + tap_u);
+                      const uint64_t ah = ah0 + koff, al = al0 + koff;
+                      for (int t = 0; t < T; ++t) {
+                        const uint32_t dt = d0 + (uint32_t)t * nacc;
+                        const uint64_t tu = (uint64_t)(t * 128);
+                        if constexpr (SCHEME == 0) {
+                          umma_tf32(dt, ah + tu, bh, idesc_cat, acc);
+                          umma_tf32(dt, al + tu, bh, idesc_one, 1u);
+                        } else {
+                          umma_tf32(dt, ah + tu, bh, idesc_one, acc);
+                          umma_tf32(dt, ah + tu, bh + b_lo_u, idesc_one, 1u);
+                          umma_tf32(dt, al + tu, bh, idesc_one, 1u);
+                        }
+                      }
+                      acc = 1u;
+                    }
+                    if (!p.resident) {
+                      umma_commit(&b_empty[rb.idx]);
+                      rb.next(p.SB);
                     }
                   }
-                  if (!p.resident) {
-                    umma_commit(&b_empty[rb.idx]);
-                    rb.next(p.SB);
-                  }
+                  if (!ok) break;
                 }
+                if (!ok) break;
               }
               if (ok && kd == 2 && ch == p.nchunks - 1) umma_commit(&acc_full[slot]);
             }
@@ -385,12 +422,17 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
   convert_done:;
   } else {
     // ------------------------------------------------------------ epilogue
+    // Two groups of four warps; each group covers all four TMEM lane quadrants and
+    // takes every other (tile, 16-channel) item of a plane.
     const int et = tid - kEpiWarp0 * 32;
-    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int q = warp & 3;                        // TMEM lane quadrant this warp may access
+    const int grp = (warp - kEpiWarp0) >> 2;       // 0 or 1
     const size_t OHW = (size_t)p.OH * p.OW;
     const int PH = p.OH / 2, PW = p.OW / 2;
-    float* s_x = s_epi;                          // pool: h-pair exchange [16][32]
-    float* s_prev = s_epi + 16 * 32;             // pool: even-plane maxima [T][Cout][32]
+    const int cchunks = p.Cout >> 4;
+    const int items = p.T * cchunks;
+    float* s_x = s_epi + grp * (16 * 32);          // pool: h-pair exchange [16][32] per group
+    float* s_prev = s_epi + 2 * (16 * 32);         // pool: even-plane maxima [T][Cout][32]
     uint32_t plane_seq = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
@@ -404,70 +446,69 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
         tc_fence_after();
         const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16) + slot * (uint32_t)(p.T * p.NACC);
         const bool pool_plane = (EPI == IG3_EPI_POOL_REDUCE) && (od / 2 < p.OD / 2);
-        for (int t = 0; t < p.T; ++t) {
+        for (int it = grp; it < items; it += 2) {
+          const int t = it / cchunks;
+          const int c0 = (it - t * cchunks) << 4;
           const int lp = t * 128 + q * 32 + lane;  // position within the unit
           const int pos = p0 + lp;
           const int oh = pos / p.W, ow = pos - oh * p.W;
           const bool valid = (oh < p.OH) && (ow < p.OW);
           const uint32_t tcol = lane_base + (uint32_t)(t * p.NACC);
-          for (int c0 = 0; c0 < p.Cout; c0 += 16) {
-            float v[16];
-            tmem_ld16(tcol + c0, v);
-            if (p.scheme == 0) {
-              float w2[16];
-              tmem_ld16(tcol + p.Cout + c0, w2);
-              tmem_wait_ld();
+          float v[16];
+          tmem_ld16(tcol + c0, v);
+          if constexpr (SCHEME == 0) {
+            float w2[16];
+            tmem_ld16(tcol + p.Cout + c0, w2);
+            tmem_wait_ld();
 #pragma unroll
-              for (int j = 0; j < 16; ++j) v[j] += w2[j];
-            } else {
-              tmem_wait_ld();
+            for (int j = 0; j < 16; ++j) v[j] += w2[j];
+          } else {
+            tmem_wait_ld();
+          }
+          if constexpr (EPI != IG3_EPI_POOL_REDUCE) {
+            float* yb = p.y + (((size_t)un.n * p.Cout + c0) * p.OD + od) * OHW + (size_t)oh * p.OW + ow;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              float val = v[j] + (p.bias ? __ldg(&p.bias[c0 + j]) : 0.0f);
+              if (EPI == IG3_EPI_TANH_MISH) val = tanh_mish(val);
+              if (valid) yb[(size_t)j * p.OD * OHW] = val;
             }
-            if constexpr (EPI != IG3_EPI_POOL_REDUCE) {
-              float* yb = p.y + (((size_t)un.n * p.Cout + c0) * p.OD + od) * OHW + (size_t)oh * p.OW + ow;
+          } else {
+            if (!pool_plane) continue;
+            // w-pair: neighbouring lanes; h-pair: position + W.
+            const int r = (q * 32 + lane) / p.W;          // row within the tile (tile rows start even)
+            const int cw = ow >> 1;
+            const int cell = (r >> 1) * (p.W >> 1) + cw;  // pooled cell within the tile, < 32
+            const bool even_w = (ow & 1) == 0, even_r = (r & 1) == 0;
+            float hm[16];
 #pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                float val = v[j] + (p.bias ? __ldg(&p.bias[c0 + j]) : 0.0f);
-                if (EPI == IG3_EPI_TANH_MISH) val = tanh_mish(val);
-                if (valid) yb[(size_t)j * p.OD * OHW] = val;
-              }
+            for (int j = 0; j < 16; ++j) {
+              const float z = (v[j] + (p.bias ? __ldg(&p.bias[c0 + j]) : 0.0f)) * p.inv_div;
+              hm[j] = fmaxf(z, __shfl_xor_sync(0xffffffffu, z, 1));
+            }
+            if (p.W <= 16) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) hm[j] = fmaxf(hm[j], __shfl_xor_sync(0xffffffffu, hm[j], p.W));
             } else {
-              if (!pool_plane) continue;
-              // w-pair: neighbouring lanes; h-pair: position + W.
-              const int r = (q * 32 + lane) / p.W;          // row within the tile (tile rows start even)
-              const int cw = ow >> 1;
-              const int cell = (r >> 1) * (p.W >> 1) + cw;  // pooled cell within the tile, < 32
-              const bool even_w = (ow & 1) == 0, even_r = (r & 1) == 0;
-              float hm[16];
+              if (!even_r && even_w) {
 #pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                const float z = (v[j] + (p.bias ? __ldg(&p.bias[c0 + j]) : 0.0f)) * p.inv_div;
-                const float wm = fmaxf(z, __shfl_xor_sync(0xffffffffu, z, 1));
-                hm[j] = wm;
+                for (int j = 0; j < 16; ++j) s_x[j * 32 + cell] = hm[j];
               }
-              if (p.W <= 16) {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) hm[j] = fmaxf(hm[j], __shfl_xor_sync(0xffffffffu, hm[j], p.W));
-              } else {
-                if (!even_r && even_w) {
-#pragma unroll
-                  for (int j = 0; j < 16; ++j) s_x[j * 32 + cell] = hm[j];
-                }
-                named_bar_sync(1, kEpiThreads);
-                if (even_r && even_w) {
-#pragma unroll
-                  for (int j = 0; j < 16; ++j) hm[j] = fmaxf(hm[j], s_x[j * 32 + cell]);
-                }
-                named_bar_sync(1, kEpiThreads);
-              }
+              named_bar_sync(1 + grp, 128);
               if (even_r && even_w) {
-                float* prev = s_prev + ((size_t)t * p.Cout + c0) * 32 + cell;
-                if ((od & 1) == 0) {
 #pragma unroll
-                  for (int j = 0; j < 16; ++j) prev[j * 32] = hm[j];
-                } else if ((oh >> 1) < PH && cw < PW) {
+                for (int j = 0; j < 16; ++j) hm[j] = fmaxf(hm[j], s_x[j * 32 + cell]);
+              }
+              named_bar_sync(1 + grp, 128);
+            }
+            if (even_r && even_w) {
+              float* prev = s_prev + ((size_t)t * p.Cout + c0) * 32 + cell;
+              if ((od & 1) == 0) {
 #pragma unroll
-                  for (int j = 0; j < 16; ++j) psum += fmaxf(prev[j * 32], hm[j]);
-                }
+                for (int j = 0; j < 16; ++j) prev[j * 32] = hm[j];
+              } else if ((oh >> 1) < PH && cw < PW) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) psum += fmaxf(prev[j * 32], hm[j]);
               }
             }
           }
@@ -477,18 +518,21 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
       }
       if (!ok) break;
       if constexpr (EPI == IG3_EPI_POOL_REDUCE) {
-        // Fixed-order reduction of the unit's partial: lanes, then warps 0..3.
+        // Fixed-order reduction of the unit's partial: lanes, then warps in order.
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, o);
-        if (lane == 0) s_red[q] = psum;
-        named_bar_sync(1, kEpiThreads);
-        if (et == 0) p.partial[u] = ((s_red[0] + s_red[1]) + s_red[2]) + s_red[3];
-        named_bar_sync(1, kEpiThreads);
+        if (lane == 0) s_red[warp - kEpiWarp0] = psum;
+        named_bar_sync(3, kEpiThreads);
+        if (et == 0) {
+          float s = 0.0f;
+          for (int i = 0; i < kEpiThreads / 32; ++i) s += s_red[i];
+          p.partial[u] = s;
+        }
+        named_bar_sync(3, kEpiThreads);
       }
       plane_seq += (uint32_t)(un.od1 - un.od0);
     }
   }
-
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -566,20 +610,23 @@ Plan make_plan(int N, int Cin, int D, int H, int W, int Cout, int epi, int grid)
       const uint32_t a_half = (uint32_t)(cc / 4) * npos * 16u;
       const uint32_t a_stage = 2 * a_half;
       const uint32_t epi_bytes =
-          (epi == IG3_EPI_POOL_REDUCE) ? (uint32_t)(16 * 32 + T * Cout * 32) * 4u : 0u;
+          (epi == IG3_EPI_POOL_REDUCE) ? (uint32_t)(2 * 16 * 32 + T * Cout * 32) * 4u : 0u;
       const uint32_t off_b = kAStages * a_stage;
       // Reserve 2 KB for static shared memory and alignment.
       const long long avail = (long long)kSmemLimit - off_b - epi_bytes - 16 * 8 - 2048;
       if (avail <= 0) continue;
       int resident = 0, sb = 0;
+      const int kss = std::max(1, std::min(cc / 8, kStageTarget / (int)bblock));
+      const uint32_t stage_bytes = (uint32_t)kss * bblock;
       if ((long long)nblocks * bblock <= avail) {
         resident = 1;
       } else {
-        sb = (int)(avail / (bblock + 16));
+        sb = (int)(avail / (stage_bytes + 16));
         if (sb < 4) continue;
         sb = std::min(sb, 64);
       }
-      const uint32_t b_bytes = resident ? nblocks * bblock : (uint32_t)sb * bblock;
+      const uint32_t b_bytes = resident ? nblocks * bblock : (uint32_t)sb * stage_bytes;
+      p.KSS = kss;
       p.T = T;
       p.NPOS = npos;
       p.CC = cc;
@@ -676,10 +723,18 @@ int conv3d_tc_launch(const Conv3dArgs& a) {
     kernel<<<grid, kThreads, pl.smem, a.stream>>>(p);
     return count_launch(cuda_status(cudaGetLastError(), "conv3d TC kernel launch"));
   };
-  switch (a.epi) {
-    case IG3_EPI_NONE: st = launch(conv3d_tc_kernel<IG3_EPI_NONE>); break;
-    case IG3_EPI_TANH_MISH: st = launch(conv3d_tc_kernel<IG3_EPI_TANH_MISH>); break;
-    default: st = launch(conv3d_tc_kernel<IG3_EPI_POOL_REDUCE>); break;
+  if (p.scheme == 0) {
+    switch (a.epi) {
+      case IG3_EPI_NONE: st = launch(conv3d_tc_kernel<IG3_EPI_NONE, 0>); break;
+      case IG3_EPI_TANH_MISH: st = launch(conv3d_tc_kernel<IG3_EPI_TANH_MISH, 0>); break;
+      default: st = launch(conv3d_tc_kernel<IG3_EPI_POOL_REDUCE, 0>); break;
+    }
+  } else {
+    switch (a.epi) {
+      case IG3_EPI_NONE: st = launch(conv3d_tc_kernel<IG3_EPI_NONE, 1>); break;
+      case IG3_EPI_TANH_MISH: st = launch(conv3d_tc_kernel<IG3_EPI_TANH_MISH, 1>); break;
+      default: st = launch(conv3d_tc_kernel<IG3_EPI_POOL_REDUCE, 1>); break;
+    }
   }
   if (st != IG3_OK || a.epi != IG3_EPI_POOL_REDUCE) return st;
   const long long cells = (long long)(p.OD / 2) * (p.OH / 2) * (p.OW / 2);
