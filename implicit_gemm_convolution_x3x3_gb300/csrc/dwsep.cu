@@ -99,12 +99,4 @@ int dwsep_fma_launch(const DwsepArgs& a) {
   return count_launch(cuda_status(cudaGetLastError(), "dwsep FMA kernel launch"));
 }
 
-const char* dwsep_tc_unsupported_reason(int, int, int, int, int) {
-  return "the tensor-core dwsep kernel is not built in this version";
-}
-
-int dwsep_tc_launch(const DwsepArgs&) {
-  return fail(IG3_ERR_UNSUPPORTED, "%s", dwsep_tc_unsupported_reason(0, 0, 0, 0, 0));
-}
-
 }  // namespace ig3
