@@ -7,7 +7,7 @@
 //   y[n,o,h,w]  = sum_c w_pw[o,c] * dw[n,c,h,w] (+ b[o])
 //
 // Tile = 128 consecutive pixels of one image row (GEMM M = 128, N = Cout, K = C).
-// Persistent CTAs (one per SM, 544 threads) walk strips of rows, so the rows above
+// Persistent CTAs (one per SM, 416 threads) walk strips of rows, so the rows above
 // and below a tile were read for the previous tile and come from L2, not HBM.
 //   warp 0      TMEM owner and MMA issuer (one thread);
 //   warps 1-8   depthwise: lane l owns pixels l, l+32, l+64, l+96 of 4 channels;
@@ -15,7 +15,7 @@
 //               right neighbours come by warp shuffle; the 3x3 sums are split into
 //               tf32 hi/lo and stored K-major [channel group][pixel][4], with
 //               consecutive lanes writing consecutive 16-byte rows (no bank conflicts);
-//   warps 9-16  epilogue: tcgen05.ld from a double-buffered TMEM accumulator,
+//   warps 9-12  epilogue: tcgen05.ld from a double-buffered TMEM accumulator,
 //               + bias, one full 128-byte line per warp store.
 // The pointwise weights are split into [hi ; lo] rows once per CTA and stay in
 // shared memory; acc = A_hi*[B_hi|B_lo] + A_lo*B_hi (3xTF32, as in conv3d_tc.cu).
@@ -30,9 +30,9 @@
 namespace ig3 {
 namespace {
 
-constexpr int kThreads = 544;
+constexpr int kThreads = 416;
 constexpr int kDwWarp0 = 1, kDwThreads = 256;
-constexpr int kEpiWarp0 = 9, kEpiThreads = 256;
+constexpr int kEpiWarp0 = 9, kEpiThreads = 128;
 constexpr int kRows = 8;        // image rows per work unit
 constexpr int kTile = 128;      // pixels per tile
 constexpr int kTmemCols = 512;
@@ -202,6 +202,24 @@ __global__ void __launch_bounds__(kThreads, 1) dwsep_tc_kernel(const DwParams p)
         const uint32_t hi_base = smem_addr(smem_a) + ra.idx * p.a_stage_bytes;
         const uint32_t lo_base = hi_base + p.a_half_bytes;
         for (int g = wd; g < groups; g += 8) {
+          // All 12 rows (4 channels x 3 image rows) of the group are loaded first so
+          // their latencies overlap; rows outside the image read as zeros (padding).
+          float v[4][3][4], el[4][3], er[4][3];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const float* xc = p.x + ((size_t)n * C + g * 4 + c) * HW;
+#pragma unroll
+            for (int dr = 0; dr < 3; ++dr) {
+              const int hh = h + dr - 1;
+              const bool rv = (hh >= 0 && hh < p.H);
+              const float* row = xc + (size_t)(rv ? hh : 0) * p.W + w0;
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                v[c][dr][k] = (rv && w0 + lane + 32 * k < p.W) ? __ldg(row + lane + 32 * k) : 0.0f;
+              el[c][dr] = (rv && w0 > 0) ? __ldg(row - 1) : 0.0f;             // pixel w0 - 1
+              er[c][dr] = (rv && w0 + kTile < p.W) ? __ldg(row + kTile) : 0.0f;  // pixel w0 + 128
+            }
+          }
           float acc[4][4];
 #pragma unroll
           for (int k = 0; k < 4; ++k)
@@ -210,29 +228,21 @@ __global__ void __launch_bounds__(kThreads, 1) dwsep_tc_kernel(const DwParams p)
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const int ch = g * 4 + c;
-            const float* xc = p.x + ((size_t)n * C + ch) * HW;
 #pragma unroll
             for (int dr = 0; dr < 3; ++dr) {
-              const int hh = h + dr - 1;
-              if (hh < 0 || hh >= p.H) continue;  // warp-uniform: zero padding rows
-              const float* row = xc + (size_t)hh * p.W + w0;
-              float v[4];
-#pragma unroll
-              for (int k = 0; k < 4; ++k) v[k] = (w0 + lane + 32 * k < p.W) ? __ldg(row + lane + 32 * k) : 0.0f;
-              const float el = (w0 > 0) ? __ldg(row - 1) : 0.0f;             // pixel w0 - 1
-              const float er = (w0 + kTile < p.W) ? __ldg(row + kTile) : 0.0f;  // pixel w0 + 128
               const float k0 = s_wdw[ch * 9 + dr * 3 + 0];
               const float k1 = s_wdw[ch * 9 + dr * 3 + 1];
               const float k2 = s_wdw[ch * 9 + dr * 3 + 2];
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
-                const float up = __shfl_up_sync(0xffffffffu, v[k], 1);
-                const float dn = __shfl_down_sync(0xffffffffu, v[k], 1);
-                const float prev_last = __shfl_sync(0xffffffffu, k > 0 ? v[k > 0 ? k - 1 : 0] : el, 31);
-                const float next_first = __shfl_sync(0xffffffffu, k < 3 ? v[k < 3 ? k + 1 : 3] : er, 0);
-                const float left = (lane == 0) ? (k > 0 ? prev_last : el) : up;
-                const float right = (lane == 31) ? (k < 3 ? next_first : er) : dn;
-                acc[k][c] = fmaf(k0, left, fmaf(k1, v[k], fmaf(k2, right, acc[k][c])));
+                const float x0 = v[c][dr][k];
+                const float up = __shfl_up_sync(0xffffffffu, x0, 1);
+                const float dn = __shfl_down_sync(0xffffffffu, x0, 1);
+                const float prev_last = __shfl_sync(0xffffffffu, k > 0 ? v[c][dr][k > 0 ? k - 1 : 0] : 0.0f, 31);
+                const float next_first = __shfl_sync(0xffffffffu, k < 3 ? v[c][dr][k < 3 ? k + 1 : 3] : 0.0f, 0);
+                const float left = (lane == 0) ? (k > 0 ? prev_last : el[c][dr]) : up;
+                const float right = (lane == 31) ? (k < 3 ? next_first : er[c][dr]) : dn;
+                acc[k][c] = fmaf(k0, left, fmaf(k1, x0, fmaf(k2, right, acc[k][c])));
               }
             }
           }
@@ -254,8 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1) dwsep_tc_kernel(const DwParams p)
   dw_done:;
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;                   // TMEM lane quadrant
-    const int grp = (warp - kEpiWarp0) >> 2;  // 0 or 1: alternate 16-column chunks
+    const int q = warp & 3;  // TMEM lane quadrant
     const int px = q * 32 + lane;
     Ring racc;
     bool ok = true;
@@ -270,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1) dwsep_tc_kernel(const DwParams p)
         tc_fence_after();
         const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + racc.idx * (uint32_t)(2 * Cout);
         float* yb = p.y + (size_t)n * Cout * HW + (size_t)h * p.W + w;
-        for (int c0 = grp * 16; c0 < Cout; c0 += 32) {
+        for (int c0 = 0; c0 < Cout; c0 += 16) {
           float v[16], v2[16];
           tmem_ld16(tb + c0, v);
           tmem_ld16(tb + Cout + c0, v2);
