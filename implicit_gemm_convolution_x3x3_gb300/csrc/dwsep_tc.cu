@@ -47,6 +47,7 @@ struct DwParams {
   int WB;         // tiles per image row
   int HR;         // row strips per image
   int units;
+  int prefetch;   // rows start on 16-byte boundaries, so bulk L2 prefetches are legal
   uint32_t a_half_bytes, a_stage_bytes, off_b, off_wdw, off_bar;
   WaitCtl ctl;
 };
@@ -201,6 +202,16 @@ __global__ void __launch_bounds__(kThreads, 1) dwsep_tc_kernel(const DwParams p)
         if (!warp_wait(&a_empty[ra.idx], ra.phase ^ 1u, p.ctl, abort_flag)) goto dw_done;
         const uint32_t hi_base = smem_addr(smem_a) + ra.idx * p.a_stage_bytes;
         const uint32_t lo_base = hi_base + p.a_half_bytes;
+        // Ask L2 now for the row the next tile reads first (h + 2), so its loads hit
+        // L2 instead of waiting on HBM: one 512-byte bulk prefetch per channel.
+        if (p.prefetch && h + 2 < p.H && lane < 8 && w0 + kTile <= p.W) {
+          const int g = wd + 8 * (lane >> 2);
+          if (g < groups) {
+            const float* src = p.x + ((size_t)n * C + g * 4 + (lane & 3)) * HW + (size_t)(h + 2) * p.W + w0;
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"((uint32_t)kTile * 4u)
+                         : "memory");
+          }
+        }
         for (int g = wd; g < groups; g += 8) {
           // All 12 rows (4 channels x 3 image rows) of the group are loaded first so
           // their latencies overlap; rows outside the image read as zeros (padding).
@@ -235,13 +246,14 @@ __global__ void __launch_bounds__(kThreads, 1) dwsep_tc_kernel(const DwParams p)
               const float k2 = s_wdw[ch * 9 + dr * 3 + 2];
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
+                // One rotate per direction: lane 31 offers the last pixel of the previous
+                // 32-pixel chunk (or the left edge) for lane 0's left neighbour, and lane 0
+                // offers the first pixel of the next chunk (or the right edge) for lane 31.
                 const float x0 = v[c][dr][k];
-                const float up = __shfl_up_sync(0xffffffffu, x0, 1);
-                const float dn = __shfl_down_sync(0xffffffffu, x0, 1);
-                const float prev_last = __shfl_sync(0xffffffffu, k > 0 ? v[c][dr][k > 0 ? k - 1 : 0] : 0.0f, 31);
-                const float next_first = __shfl_sync(0xffffffffu, k < 3 ? v[c][dr][k < 3 ? k + 1 : 3] : 0.0f, 0);
-                const float left = (lane == 0) ? (k > 0 ? prev_last : el[c][dr]) : up;
-                const float right = (lane == 31) ? (k < 3 ? next_first : er[c][dr]) : dn;
+                const float lsrc = (lane == 31) ? (k > 0 ? v[c][dr][k > 0 ? k - 1 : 0] : el[c][dr]) : x0;
+                const float rsrc = (lane == 0) ? (k < 3 ? v[c][dr][k < 3 ? k + 1 : 3] : er[c][dr]) : x0;
+                const float left = __shfl_sync(0xffffffffu, lsrc, (lane + 31) & 31);
+                const float right = __shfl_sync(0xffffffffu, rsrc, (lane + 1) & 31);
                 acc[k][c] = fmaf(k0, left, fmaf(k1, x0, fmaf(k2, right, acc[k][c])));
               }
             }
@@ -371,6 +383,7 @@ int dwsep_tc_launch(const DwsepArgs& a) {
   p.w_pw = a.w_pw;
   p.bias = a.b;
   p.y = a.y;
+  p.prefetch = (a.W % 4 == 0) && (reinterpret_cast<uintptr_t>(a.x) % 16 == 0);
   p.ctl = wait_ctl();
   if (!p.ctl.status) return fail(IG3_ERR_CUDA, "dwsep TC path: device status word unavailable");
   cudaError_t e = cudaFuncSetAttribute(dwsep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
