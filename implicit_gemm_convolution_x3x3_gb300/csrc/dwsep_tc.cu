@@ -215,7 +215,11 @@ __global__ void __launch_bounds__(kThreads, 1) dwsep_tc_kernel(const DwParams p)
         for (int g = wd; g < groups; g += 8) {
           // All 12 rows (4 channels x 3 image rows) of the group are loaded first so
           // their latencies overlap; rows outside the image read as zeros (padding).
-          float v[4][3][4], el[4][3], er[4][3];
+          // edge[c][dr]: lane 0 holds pixel w0 - 1 and lane 31 pixel w0 + 128 (one load
+          // instruction for both ends of the row segment; other lanes hold zero).
+          float v[4][3][4], edge[4][3];
+          const bool edge_lane = (lane == 0) ? (w0 > 0) : (lane == 31 && w0 + kTile < p.W);
+          const int edge_off = (lane == 0) ? -1 : kTile;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const float* xc = p.x + ((size_t)n * C + g * 4 + c) * HW;
@@ -227,8 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1) dwsep_tc_kernel(const DwParams p)
 #pragma unroll
               for (int k = 0; k < 4; ++k)
                 v[c][dr][k] = (rv && w0 + lane + 32 * k < p.W) ? __ldg(row + lane + 32 * k) : 0.0f;
-              el[c][dr] = (rv && w0 > 0) ? __ldg(row - 1) : 0.0f;             // pixel w0 - 1
-              er[c][dr] = (rv && w0 + kTile < p.W) ? __ldg(row + kTile) : 0.0f;  // pixel w0 + 128
+              edge[c][dr] = (rv && edge_lane) ? __ldg(row + edge_off) : 0.0f;
             }
           }
           float acc[4][4];
@@ -250,10 +253,14 @@ __global__ void __launch_bounds__(kThreads, 1) dwsep_tc_kernel(const DwParams p)
                 // 32-pixel chunk (or the left edge) for lane 0's left neighbour, and lane 0
                 // offers the first pixel of the next chunk (or the right edge) for lane 31.
                 const float x0 = v[c][dr][k];
-                const float lsrc = (lane == 31) ? (k > 0 ? v[c][dr][k > 0 ? k - 1 : 0] : el[c][dr]) : x0;
-                const float rsrc = (lane == 0) ? (k < 3 ? v[c][dr][k < 3 ? k + 1 : 3] : er[c][dr]) : x0;
-                const float left = __shfl_sync(0xffffffffu, lsrc, (lane + 31) & 31);
-                const float right = __shfl_sync(0xffffffffu, rsrc, (lane + 1) & 31);
+                // Edge pixels: lane 0's left end (held by lane 0) and lane 31's right end
+                // (held by lane 31) are used by the same lane, so they bypass the shuffle.
+                const float lsrc = (lane == 31) ? (k > 0 ? v[c][dr][k > 0 ? k - 1 : 0] : 0.0f) : x0;
+                const float rsrc = (lane == 0) ? (k < 3 ? v[c][dr][k < 3 ? k + 1 : 3] : 0.0f) : x0;
+                float left = __shfl_sync(0xffffffffu, lsrc, (lane + 31) & 31);
+                float right = __shfl_sync(0xffffffffu, rsrc, (lane + 1) & 31);
+                if (k == 0 && lane == 0) left = edge[c][dr];
+                if (k == 3 && lane == 31) right = edge[c][dr];
                 acc[k][c] = fmaf(k0, left, fmaf(k1, x0, fmaf(k2, right, acc[k][c])));
               }
             }
