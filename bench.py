@@ -57,6 +57,14 @@ WORKLOADS = {
 }
 
 
+def with_batch(wl, n: int):
+    """The same workload with batch size n (same seed and distributions)."""
+    import dataclasses
+    tensors = [dataclasses.replace(t, shape=(n,) + tuple(t.shape[1:])) if t.name == "x" else t
+               for t in wl.tensors]
+    return dataclasses.replace(wl, name=f"{wl.name}_batch{n}", tensors=tensors)
+
+
 # ------------------------------------------------------------------ workload arithmetic
 def macs(wl) -> int:
     d = wl.dims
@@ -429,7 +437,8 @@ def run_ours(args) -> None:
         "config": {"workload": describe(wl), "name": wl.name, "global_batch": wl.dims["N"] * world,
                    "path": res["path"], "arith": ("3xTF32 on tcgen05 tensor cores, fp32 accumulate"
                                                   if res["path"] == "tc" else "fp32 FMA"),
-                   "l2": ("inputs larger than L2 (%.0f MB read, %.0f MB written per step; L2 %d MB)"
+                   "l2": (("inputs larger than L2" if rd > L2_BYTES else "working set NOT larger than L2 (no flush)")
+                          + " (%.0f MB read, %.0f MB written per step; L2 %d MB)"
                           % (rd / 1e6, wr / 1e6, L2_BYTES // 2**20)),
                    "parallelism": f"batch shard per GPU x{world}" if world > 1 else "single GPU",
                    "us_per_call": res["us_per_call"]},
@@ -480,7 +489,12 @@ def main():
     ap.add_argument("--no-others", action="store_true", help="skip the other workloads' summary")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample size in seconds")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch size (smaller cases for profiling; not a bench line)")
     args = ap.parse_args()
+    if args.batch > 0:
+        base = WORKLOADS[args.workload]
+        WORKLOADS[args.workload] = lambda: with_batch(base(), args.batch)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
