@@ -19,25 +19,34 @@
 // Precision.  fp32 operands are split into hi (tf32-exact, low 13 bits cleared) and
 // lo = x - hi; the tensor core truncates operands to tf32, so hi is exact and
 //   acc += A_hi*B_hi + A_hi*B_lo + A_lo*B_hi
-// keeps the product to about 2^-21 relative with fp32 accumulation.  For
-// Cout <= 64 the first two terms are one MMA with B = [B_hi ; B_lo] (N = 2*Cout)
-// into 2*Cout accumulator columns (summed in the epilogue) and the third is a
-// second MMA into the first Cout columns; for Cout > 64 three MMAs of N = Cout.
+// keeps the product to about 2^-21 relative with fp32 accumulation.  Each of the
+// three products is one MMA into the same accumulator columns.
+//
+// Window MMAs.  Input plane d feeds output planes d-2, d-1, d through the kd = 2, 1, 0
+// weights.  One thread can issue a tcgen05.mma only every ~46 cycles, so small MMAs
+// leave the tensor pipe idle; instead the accumulators of consecutive output planes
+// sit in adjacent TMEM slots (Cout columns each) and the weights of one (kh, kw) tap
+// are stored with rows [kd=2 | kd=1 | kd=0], so ONE MMA with N = 3*Cout applies all
+// three kd of an input plane (KDM 3, Cout <= 80).  A unit's P output planes use slots
+// 0..P-1, so the window never wraps; planes at the ends of a unit use the sub-window
+// of the kd that fall inside it.  Every MMA accumulates: the slots start at zero and
+// the epilogue zeroes each slot after reading it.  For Cout > 80 (3*Cout > 256, the
+// largest N) each kd is its own MMA (KDM 1) and the slots form a ring.
 //
 // Data flow (persistent CTAs, one per SM, 512 threads, warp-specialised):
-//   warp 0      weight producer: 1-D bulk copies (TMA) of pre-split K-step blocks
-//               [hi rows ; lo rows] from the workspace into a ring of stages (one
-//               stage = the K-steps of one tap, up to 16 KB), or all blocks once
-//               when they fit (resident weights);
+//   warp 0      weight producer: 1-D bulk copies (TMA) of pre-split K-step blocks from
+//               the workspace into a ring of stages (one stage = one tap's K-steps of
+//               one channel chunk), or all blocks once when they fit (resident);
 //   warp 1      TMEM owner and MMA issuer (one thread; descriptors are formed once
-//               and advanced by adds, which keeps issue at the tensor pipe's rate);
+//               and advanced by adds; the nine taps are unrolled);
 //   warps 2-7   input convert: coalesced loads of x, hi/lo split, K-major stores;
 //   warps 8-15  epilogue, two groups of four (one warp per TMEM lane quadrant each):
-//               tcgen05.ld, bias, activation or pool-reduce, stores.
-// A work unit is (batch item n, group of T position tiles, range of output
-// planes).  Input planes stream through a 2-stage A buffer; each input plane d
-// feeds output planes d, d-1, d-2 (kd = 0, 1, 2), whose accumulators live in a
-// 4-slot TMEM ring, so the epilogue of one plane overlaps the MMAs of the next.
+//               tcgen05.ld, zeroing tcgen05.st, bias, activation or pool-reduce, stores.
+// A work unit is (batch item n, group of T position tiles, range of P output planes).
+// Input planes stream through a 2-stage A buffer (one channel chunk per stage), so
+// the convert of the next chunk and the epilogue of finished planes overlap the MMAs.
+// The plan (T, chunk size, resident or streamed weights, P) comes from a cycle model
+// of the issue and execution rates above and of the persistent schedule.
 //
 // Pool-reduce ("Kimi-K2.6__l2_p8": /divisor, MaxPool3d(2) floor mode, global mean,
 // +bias2, sum over channels): TMEM lane = position, so the w-pair max is a lane
@@ -49,9 +58,12 @@
 // Every wait is bounded (ig3_device.cuh); on a timeout all roles stop, in-flight
 // copies and MMAs are drained and TMEM is freed before the CTA exits.
 #include <algorithm>
+#include <array>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <map>
+#include <mutex>
 
 #include "conv3d_tc_kernel.cuh"
 
@@ -60,27 +72,44 @@ namespace {
 
 using namespace tc;
 
-// Weights [Cout][Cin][27] -> K-step blocks [tap][KS][khalf][2*Cout rows][4]:
-// rows 0..Cout-1 hold the tf32 hi part, rows Cout..2*Cout-1 the lo part; channels
-// past Cin are zero.
+// Weights [Cout][Cin][27] -> pre-split K-step blocks, each [khalf][rows][4] (rows
+// of 4 consecutive channels, the two channel halves of the K-step one after the
+// other), channels past Cin zero:
+//   KDM 3: block (khw * KS + ks), rows [hi kd=2 | hi kd=1 | hi kd=0 | lo kd=2 | lo kd=1 |
+//          lo kd=0] x Cout, so any run of adjacent kd is a contiguous row range;
+//   KDM 1: block ((kd * 9 + khw) * KS + ks), rows [hi | lo] x Cout.
+// khw = kh * 3 + kw.  Both layouts hold 27 * KS * 2 * 2*Cout * 4 floats.
 __global__ void conv3d_tc_prep_weights(const float* __restrict__ w, float* __restrict__ blob, int Cin, int Cout,
-                                       int KS) {
+                                       int KS, int kdm) {
+  const int rows = (kdm == 3 ? 6 : 2) * Cout;
   const int total = 27 * KS * 2 * (2 * Cout) * 4;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
     const int j = i & 3;
     int r = i >> 2;
-    const int row = r % (2 * Cout);
-    r /= 2 * Cout;
-    const int kh = r & 1;
+    const int row = r % rows;
+    r /= rows;
+    const int khalf = r & 1;
     r >>= 1;
     const int ks = r % KS;
-    const int tap = r / KS;
-    const int c = ks * 8 + kh * 4 + j;
-    const int co = row % Cout;
-    float v = (c < Cin) ? w[((size_t)co * Cin + c) * 27 + tap] : 0.0f;
-    float hi, lo;
-    split_tf32(v, hi, lo);
-    blob[i] = (row < Cout) ? hi : lo;
+    const int blk = r / KS;
+    int tap, co;
+    bool hi;
+    if (kdm == 3) {
+      hi = row < 3 * Cout;
+      const int rr = hi ? row : row - 3 * Cout;
+      const int kd = 2 - rr / Cout;
+      co = rr % Cout;
+      tap = kd * 9 + blk;  // blk = khw
+    } else {
+      hi = row < Cout;
+      co = hi ? row : row - Cout;
+      tap = blk;           // blk = kd * 9 + khw
+    }
+    const int c = ks * 8 + khalf * 4 + j;
+    const float v = (c < Cin) ? w[((size_t)co * Cin + c) * 27 + tap] : 0.0f;
+    float h, l;
+    split_tf32(v, h, l);
+    blob[i] = hi ? h : l;
   }
 }
 
@@ -95,10 +124,31 @@ struct Plan {
 
 int positions_tiles(int OH, int W, int T) { return ((OH * W) + T * 128 - 1) / (T * 128); }
 
-Plan make_plan(int N, int Cin, int D, int H, int W, int Cout, int epi, int grid) {
+// Cycle estimate of one input plane's MMAs (per SM): nkd output planes fed, per
+// (tap, K-step, tile) three MMAs.  A tcgen05.mma takes ~46 cycles to issue from one
+// thread and N/2 cycles to execute (M = 128, K = 8, N >= 96); every streamed weight
+// stage adds ~250 cycles of wait and commit to the issuing thread.
+double plane_cycles(int kdm, int nkd, int Cout, int KS, int nchunks, int T, bool res) {
+  const double issue_one = 46.0;
+  const int mmas_per_step = (kdm == 3) ? 3 : 3 * nkd;
+  const int n = (kdm == 3) ? nkd * Cout : Cout;
+  const double exec = 9.0 * KS * T * mmas_per_step * std::max(issue_one, 0.5 * n);
+  const double stages = res ? 0.0 : 9.0 * nchunks * (kdm == 3 ? 1 : nkd);
+  const double issue = 9.0 * KS * T * mmas_per_step * issue_one + 250.0 * stages;
+  return std::max(exec, issue) + 300.0 * nchunks;  // A hand-over per chunk
+}
+
+double unit_cycles(int kdm, int planes, int Cout, int KS, int nchunks, int T, bool res) {
+  double c = 0.0;
+  for (int d = 0; d < planes + 2; ++d) {
+    const int kd_hi = std::min(2, d), kd_lo = std::max(0, d - planes + 1);
+    c += plane_cycles(kdm, kd_hi - kd_lo + 1, Cout, KS, nchunks, T, res);
+  }
+  return c;
+}
+
+Plan make_plan_uncached(int N, int Cin, int D, int H, int W, int Cout, int epi, int sms) {
   Plan pl;
-  TcParams& p = pl.prm;
-  std::memset(&p, 0, sizeof(p));
   if (Cout % 16 != 0 || Cout > 128) {
     pl.why = "Cout must be a multiple of 16 and at most 128";
     return pl;
@@ -111,93 +161,114 @@ Plan make_plan(int N, int Cin, int D, int H, int W, int Cout, int epi, int grid)
     pl.why = "W above 1024";
     return pl;
   }
-  p.N = N; p.Cin = Cin; p.D = D; p.H = H; p.W = W; p.Cout = Cout;
-  p.OD = D - 2; p.OH = H - 2; p.OW = W - 2;
-  p.epi = epi;
-  p.scheme = (Cout <= 64) ? 0 : 1;
-  p.NACC = (p.scheme == 0) ? 2 * Cout : Cout;
-  p.KS = (Cin + 7) / 8;
-  const int tmax = std::max(1, std::min(4, kTmemCols / (kSlots * p.NACC)));
-  const uint32_t bblock = 64u * (uint32_t)Cout;
-  const int nblocks = 27 * p.KS;
-  bool found = false;
-  for (int T = tmax; T >= 1 && !found; --T) {
+  const int OD = D - 2, OH = H - 2;
+  const int kdm = (3 * Cout <= 256) ? 3 : 1;
+  const int ks0 = (Cin + 7) / 8;
+  const int step = (epi == IG3_EPI_POOL_REDUCE) ? 2 : 1;
+  double best = 1e300;
+  for (const Variant& v : kVariants) {
+    if (v.kdm != kdm) continue;
+    const int T = v.t, kss = v.kss;
+    const bool res = v.res != 0;
+    const int KS = (ks0 + kss - 1) / kss * kss;
+    const int nchunks = KS / kss;
+    const int nslot = std::min(kMaxSlots, kTmemCols / (T * Cout));
+    if (nslot < (kdm == 3 ? step : 4)) continue;
     const int npos = ((T * 128 + 2 * W + 2) + 7) / 8 * 8;
-    for (int cc : {32, 24, 16, 8}) {
-      if (cc > p.KS * 8) continue;
-      const uint32_t a_half = (uint32_t)(cc / 4) * npos * 16u;
-      const uint32_t a_stage = 2 * a_half;
-      const uint32_t epi_bytes =
-          (epi == IG3_EPI_POOL_REDUCE) ? (uint32_t)(2 * 16 * 32 + T * Cout * 32) * 4u : 0u;
-      const uint32_t off_b = kAStages * a_stage;
-      // Reserve 2 KB for static shared memory and alignment.
-      const long long avail = (long long)kSmemLimit - off_b - epi_bytes - 16 * 8 - 2048;
-      if (avail <= 0) continue;
-      int resident = 0, sb = 0;
-      // K-steps per weight stage: a power of two (1, 2 or 4) within kStageTarget
-      // bytes that divides the K-steps of every channel chunk (the last may be short).
-      const int last_ks = (p.KS * 8 - ((p.KS * 8 + cc - 1) / cc - 1) * cc) / 8;
-      int kss = 4;
-      while (kss > 1 && (kss * (int)bblock > kStageTarget || (cc / 8) % kss != 0 || last_ks % kss != 0)) kss >>= 1;
-      const uint32_t stage_bytes = (uint32_t)kss * bblock;
-      if ((long long)nblocks * bblock <= avail) {
-        resident = 1;
-      } else {
-        sb = (int)(avail / (stage_bytes + 16));
-        if (sb < 4) continue;
-        sb = std::min(sb, 64);
+    const uint32_t a_half = (uint32_t)(2 * kss) * npos * 16u;
+    const uint32_t a_stage = 2 * a_half;
+    const uint32_t blk = (uint32_t)((kdm == 3 ? 192 : 64) * Cout);
+    const uint32_t blob = (uint32_t)(1728 * KS * Cout);
+    const uint32_t epi_bytes = (epi == IG3_EPI_POOL_REDUCE) ? (uint32_t)(2 * 16 * 32 + T * Cout * 32) * 4u : 0u;
+    const uint32_t off_b = kAStages * a_stage;
+    // 2 KB for static shared memory and alignment; barriers for the largest ring.
+    const long long avail =
+        (long long)kSmemLimit - off_b - epi_bytes - 2048 - 128 - (6 + 2 * nslot + 2 * kMaxStages) * 8;
+    if (avail <= 0) continue;
+    int sb = 0;
+    if (res) {
+      if ((long long)blob > avail) continue;
+    } else {
+      sb = (int)std::min<long long>(kMaxStages, avail / ((long long)kss * blk));
+      if (sb < 3) continue;
+    }
+    // Planes per unit: with KDM 3 a unit's planes must fit the slots.
+    const int pmax = (kdm == 3) ? std::min(OD, nslot) : OD;
+    const int G = positions_tiles(OH, W, T);
+    for (int P = pmax - (pmax % step == 0 ? 0 : 1); P >= step; P -= step) {
+      const int S = (OD + P - 1) / P;
+      const int last = OD - (S - 1) * P;
+      const long long units = (long long)N * G * S;
+      const int grid = (int)std::min<long long>(units, sms);
+      const double c_full = unit_cycles(kdm, P, Cout, KS, nchunks, T, res);
+      const double c_last = unit_cycles(kdm, last, Cout, KS, nchunks, T, res);
+      // Round-robin over the grid: CTA c takes units c, c + grid, ...; a unit is
+      // the last split iff u % S == S - 1.
+      double worst = 0.0;
+      for (int c = 0; c < grid; ++c) {
+        double t = 0.0;
+        for (long long u = c; u < units; u += grid) t += (u % S == S - 1) ? c_last : c_full;
+        worst = std::max(worst, t);
       }
-      const uint32_t b_bytes = resident ? nblocks * bblock : (uint32_t)sb * stage_bytes;
-      p.KSS = kss;
-      p.T = T;
-      p.NPOS = npos;
-      p.CC = cc;
-      p.nchunks = (p.KS * 8 + cc - 1) / cc;
-      p.a_half_bytes = a_half;
-      p.a_stage_bytes = a_stage;
-      p.b_block_bytes = bblock;
-      p.resident = resident;
-      p.SB = sb;
-      p.off_b = off_b;
-      p.off_epi = off_b + b_bytes;
-      p.off_bar = (p.off_epi + epi_bytes + 127) / 128 * 128;
-      pl.smem = p.off_bar + (16 + 2 * (size_t)sb) * 8;
-      if (pl.smem > (size_t)kSmemLimit) continue;
-      found = true;
-      break;
+      if (worst < best * (1.0 - 1e-9)) {
+        best = worst;
+        TcParams& p = pl.prm;
+        std::memset(&p, 0, sizeof(p));
+        p.N = N; p.Cin = Cin; p.D = D; p.H = H; p.W = W; p.Cout = Cout;
+        p.OD = OD; p.OH = OH; p.OW = W - 2;
+        p.epi = epi;
+        p.KS = KS;
+        p.KSS = kss;
+        p.nchunks = nchunks;
+        p.T = T;
+        p.NPOS = npos;
+        p.KDM = kdm;
+        p.NSLOT = nslot;
+        p.G = G;
+        p.S = S;
+        p.P = P;
+        p.units = (int)units;
+        p.resident = res ? 1 : 0;
+        p.SB = sb;
+        p.a_half_bytes = a_half;
+        p.a_stage_bytes = a_stage;
+        p.b_block_bytes = blk;
+        p.off_b = off_b;
+        p.off_epi = off_b + (res ? blob : (uint32_t)sb * kss * blk);
+        p.off_bar = (p.off_epi + epi_bytes + 127) / 128 * 128;
+        pl.smem = std::max<size_t>(p.off_bar + (6 + 2 * (size_t)nslot + 2 * (size_t)sb) * 8, kMinSmem);
+        pl.ok = true;
+      }
     }
   }
-  if (!found) {
+  if (!pl.ok) {
     pl.why = "no tiling fits in shared memory";
     return pl;
   }
-  p.G = positions_tiles(p.OH, W, p.T);
-  // Split the output planes so the units fill the grid evenly; each extra split
-  // costs about 2 input planes of conversion and pipeline fill (weight 0.3 each).
-  const int step = (epi == IG3_EPI_POOL_REDUCE) ? 2 : 1;
-  double best = 1e30;
-  int bestS = 1, bestP = p.OD;
-  for (int P = p.OD + (p.OD % step); P >= step; P -= step) {
-    const int S = (p.OD + P - 1) / P;
-    const long long units = (long long)N * p.G * S;
-    const long long waves = (units + grid - 1) / grid;
-    const double cost = (double)waves * (P + 0.6);
-    if (cost < best - 1e-9) {
-      best = cost;
-      bestS = S;
-      bestP = P;
-    }
+  // Sizes that do not depend on the plan (nor on the device): the blob padded to a
+  // multiple of 4 K-steps, partials for the finest possible split.
+  pl.blob_bytes = align_up((size_t)1728 * ((ks0 + 3) / 4 * 4) * Cout, 256);
+  pl.partial_bytes =
+      (epi == IG3_EPI_POOL_REDUCE) ? align_up((size_t)N * positions_tiles(OH, W, 1) * OD * sizeof(float), 256) : 0;
+  return pl;
+}
+
+// Plans are cached per (shape, epilogue, SM count): the search above simulates the
+// persistent schedule and is not free.
+Plan make_plan(int N, int Cin, int D, int H, int W, int Cout, int epi, int sms) {
+  using Key = std::array<int, 8>;
+  static std::mutex mu;
+  static std::map<Key, Plan> cache;
+  const Key key{N, Cin, D, H, W, Cout, epi, sms};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
   }
-  p.S = bestS;
-  p.P = bestP;
-  p.units = N * p.G * p.S;
-  pl.blob_bytes = align_up((size_t)nblocks * bblock, 256);
-  // Upper bound over any split, so the size query does not depend on the device.
-  pl.partial_bytes = (epi == IG3_EPI_POOL_REDUCE)
-                         ? align_up((size_t)N * positions_tiles(p.OH, W, p.T) * p.OD * sizeof(float), 256)
-                         : 0;
-  pl.smem = std::max(pl.smem, (size_t)kMinSmem);
-  pl.ok = true;
+  Plan pl = make_plan_uncached(N, Cin, D, H, W, Cout, epi, sms);
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache.size() > 256) cache.clear();
+  cache.emplace(key, pl);
   return pl;
 }
 
@@ -234,7 +305,7 @@ int conv3d_tc_launch(const Conv3dArgs& a) {
 
   const int total = 27 * p.KS * 2 * (2 * p.Cout) * 4;
   conv3d_tc_prep_weights<<<std::min((total + 255) / 256, 4 * sms), 256, 0, a.stream>>>(
-      a.w, const_cast<float*>(p.wblob), a.Cin, a.Cout, p.KS);
+      a.w, const_cast<float*>(p.wblob), a.Cin, a.Cout, p.KS, p.KDM);
   int st = count_launch(cuda_status(cudaGetLastError(), "conv3d TC weight prep launch"));
   if (st != IG3_OK) return st;
 

@@ -10,36 +10,34 @@
 namespace ig3 {
 namespace tc {
 
-
 constexpr int kThreads = 512;
 constexpr int kConvWarp0 = 2, kConvThreads = 192;
 constexpr int kEpiWarp0 = 8, kEpiThreads = 256;  // two warps per TMEM lane quadrant
-constexpr int kStageTarget = 16 * 1024;           // bytes of weights per ring stage
-constexpr int kSlots = 4;
 constexpr int kAStages = 2;
 constexpr int kTmemCols = 512;
+constexpr int kMaxSlots = 32;  // accumulator slots per position tile (one parity bit each)
+constexpr int kMaxStages = 8;  // weight ring stages
 constexpr int kSmemLimit = 227 * 1024;
 constexpr int kMinSmem = 116 * 1024;  // keeps one CTA (one TMEM owner) per SM
 
 struct TcParams {
   const float* x;
-  const float* wblob;  // [27 taps][KS K-steps][2 k-halves][2*Cout rows][4]
+  const float* wblob;  // pre-split weight blocks, layout set by KDM (see conv3d_tc.cu)
   const float* bias;
   float* y;
   float* partial;
   int N, Cin, D, H, W, Cout, OD, OH, OW;
-  int KS;        // K-steps of 8 channels over the padded Cin
-  int CC;        // channels per A chunk (multiple of 8)
-  int nchunks;
+  int KS;        // K-steps of 8 channels over the padded Cin (a multiple of KSS)
+  int KSS;       // K-steps per channel chunk (= per weight stage)
+  int nchunks;   // KS / KSS
   int T;         // position tiles of 128 per unit
   int NPOS;      // positions held per A stage
-  int NACC;      // accumulator columns per tile
-  int scheme;    // 0: [hi;lo] B + 1 MMA for lo (Cout <= 64); 1: three MMAs
-  int G, S, P;   // tile groups per plane, plane splits, planes per split
+  int KDM;       // 3: one MMA spans the kd = 2, 1, 0 accumulators; 1: one MMA per kd
+  int NSLOT;     // accumulator slots per tile, Cout columns each
+  int G, S, P;   // tile groups per plane, plane splits, output planes per split
   int units;
   int resident;  // weights loaded once
   int SB;        // weight ring stages (streaming)
-  int KSS;       // K-step blocks per ring stage (all of one tap, up to kStageTarget bytes)
   int epi;
   float inv_div;
   uint32_t a_half_bytes;   // one of hi / lo in an A stage
@@ -63,7 +61,7 @@ struct Unit {
   int n, g, od0, od1;
 };
 
-static __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
+static __host__ __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
   Unit r;
   const int s = u % p.S;
   const int g = (u / p.S) % p.G;
@@ -74,8 +72,16 @@ static __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
   return r;
 }
 
-static __device__ __forceinline__ int chunk_channels(const TcParams& p, int ch) {
-  return min(p.CC, p.KS * 8 - ch * p.CC);
+// First accumulator slot of a unit: with KDM 3 every unit starts at slot 0 (its P
+// planes fit in the slots, so a window of adjacent planes never wraps); with KDM 1
+// the slots form a ring that runs on across units.
+static __host__ __device__ __forceinline__ uint32_t unit_slot0(const TcParams& p, uint32_t plane_seq) {
+  return p.KDM == 3 ? 0u : plane_seq % (uint32_t)p.NSLOT;
+}
+
+// Slot of the unit's k-th output plane (k >= 0; with KDM 1, k may exceed NSLOT).
+static __host__ __device__ __forceinline__ uint32_t slot_add(const TcParams& p, uint32_t s0, int k) {
+  return (s0 + (uint32_t)k) % (uint32_t)p.NSLOT;
 }
 
 // A bounded wait used while shutting down: ignores the abort flag.
@@ -91,8 +97,7 @@ static __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity,
   return __all_sync(0xffffffffu, ok) != 0;
 }
 
-// Non-blocking test of a barrier phase (try_wait may suspend the thread for a while
-// even when it returns true at once; test_wait never does).
+// Non-blocking test of a barrier phase.
 static __device__ __forceinline__ bool mbar_test_wait(uint32_t bar_addr, uint32_t parity) {
   uint32_t done;
   asm volatile(
@@ -110,33 +115,67 @@ static __device__ __forceinline__ bool wait_fast(uint64_t* bar, uint32_t parity,
   return mbar_wait_bounded(bar, parity, ctl, abort);
 }
 
-// The MMAs of one weight stage: KSS K-steps x T position tiles, fully unrolled so the
-// issue is a straight run of adds and tcgen05.mma.  `acc` is 0 only for the first
-// K-step of a plane (it overwrites the accumulator) and 1 afterwards.
-template <int SCHEME, int T, int KSS>
-static __device__ __forceinline__ void issue_stage(uint32_t d0, uint64_t ah0, uint64_t al0, uint64_t bst,
-                                                   uint32_t koff0, uint32_t ks_u, uint32_t b_block_u,
-                                                   uint32_t b_lo_u, uint32_t nacc, uint32_t idesc_cat,
-                                                   uint32_t idesc_one, uint32_t& acc) {
+// The MMAs of one weight stage (KSS K-steps x T position tiles), fully unrolled so
+// the issue is a straight run of adds and tcgen05.mma.  Each product of the split
+// (A_hi B_hi, A_hi B_lo, A_lo B_hi) is one MMA into the same accumulator columns;
+// the accumulators start at zero, so every MMA accumulates.
+//   dcol      first accumulator column of tile 0
+//   ah0, al0  A descriptors (hi, lo) of this A stage, tap offset included
+//   bh0       B descriptor of the stage's first K-step, hi rows of the window
+//   lo_u      distance from hi rows to lo rows (16-byte units)
+template <int T, int KSS>
+static __device__ __forceinline__ void issue_stage(uint32_t dcol, uint32_t tile_cols, uint64_t ah0, uint64_t al0,
+                                                   uint64_t bh0, uint32_t lo_u, uint32_t ks_u, uint32_t blk_u,
+                                                   uint32_t idesc) {
 #pragma unroll
   for (int j = 0; j < KSS; ++j) {
-    const uint64_t bh = bst + (uint64_t)(j * b_block_u);
-    const uint64_t koff = (uint64_t)(koff0 + (uint32_t)j * ks_u);
+    const uint64_t bh = bh0 + (uint64_t)(j * blk_u);
+    const uint64_t bl = bh + lo_u;
+    const uint64_t koff = (uint64_t)((uint32_t)j * ks_u);
 #pragma unroll
     for (int t = 0; t < T; ++t) {
-      const uint32_t dt = d0 + (uint32_t)t * nacc;
+      const uint32_t dt = dcol + (uint32_t)t * tile_cols;
       const uint64_t ah = ah0 + koff + (uint64_t)(t * 128), al = al0 + koff + (uint64_t)(t * 128);
-      if constexpr (SCHEME == 0) {
-        umma_tf32(dt, ah, bh, idesc_cat, acc);
-        umma_tf32(dt, al, bh, idesc_one, 1u);
+      umma_tf32(dt, ah, bh, idesc, 1u);
+      umma_tf32(dt, ah, bl, idesc, 1u);
+      umma_tf32(dt, al, bh, idesc, 1u);
+    }
+  }
+}
+
+// All nine (kh, kw) taps of one A chunk against one set of accumulator columns.
+// Streaming weights: one ring stage per tap, waited for, used and released.
+// Resident weights: block (tap_base + khw) * KS + blk0.  Returns false if a wait gave
+// up (the MMAs are still issued, on whatever the buffers hold; the caller stops).
+template <int T, int KSS, bool RES>
+static __device__ __forceinline__ bool issue_taps(const TcParams& p, uint32_t dcol, uint32_t tile_cols,
+                                                  uint64_t ah0, uint64_t al0, uint64_t bwin, uint32_t lo_u,
+                                                  uint32_t ks_u, uint32_t blk_u, uint32_t row_u, uint32_t idesc,
+                                                  int tap_base, int blk0, uint64_t* b_full, uint64_t* b_empty,
+                                                  Ring& rb, volatile int* abort_flag) {
+  bool good = true;
+  const uint32_t b_stage_u = blk_u * (uint32_t)KSS;
+#pragma unroll
+  for (int kh = 0; kh < 3; ++kh) {
+#pragma unroll
+    for (int kw = 0; kw < 3; ++kw) {
+      const uint64_t tap_u = (uint64_t)((uint32_t)kh * row_u + (uint32_t)kw);
+      uint64_t bst;
+      if constexpr (RES) {
+        bst = bwin + (uint64_t)((uint32_t)((tap_base + kh * 3 + kw) * p.KS + blk0) * blk_u);
       } else {
-        umma_tf32(dt, ah, bh, idesc_one, acc);
-        umma_tf32(dt, ah, bh + b_lo_u, idesc_one, 1u);
-        umma_tf32(dt, al, bh, idesc_one, 1u);
+        if (!wait_fast(&b_full[rb.idx], rb.phase, p.ctl, abort_flag)) good = false;
+        tc_fence_after();
+        bst = bwin + (uint64_t)(rb.idx * b_stage_u);
+      }
+      issue_stage<T, KSS>(dcol, tile_cols, ah0 + tap_u, al0 + tap_u, bst, lo_u, ks_u, blk_u, idesc);
+      if constexpr (!RES) {
+        umma_commit(&b_empty[rb.idx]);
+        rb.next((uint32_t)p.SB);
       }
     }
-    acc = 1u;
   }
+  return good;
 }
 
 static __device__ __forceinline__ void named_bar_sync(int id, int count) {
@@ -147,7 +186,7 @@ static __device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, floa
   asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
-template <int EPI, int SCHEME, int T, int KSS>
+template <int EPI, int KDM, int T, int KSS, bool RES>
 __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ uint32_t s_tmem;
@@ -158,18 +197,19 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
   uint8_t* smem_b = smem + p.off_b;
   float* s_epi = reinterpret_cast<float*>(smem + p.off_epi);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
-  uint64_t* a_full = bars;                   // [2]
-  uint64_t* a_empty = bars + 2;              // [2]
-  uint64_t* acc_full = bars + 4;             // [4]
-  uint64_t* acc_empty = bars + 8;            // [4]
-  uint64_t* w_full = bars + 12;              // resident weights
-  uint64_t* mma_done = bars + 13;            // final drain of the MMA pipe
-  uint64_t* b_full = bars + 16;              // [SB]
-  uint64_t* b_empty = bars + 16 + p.SB;      // [SB]
+  uint64_t* a_full = bars;                     // [2]
+  uint64_t* a_empty = bars + 2;                // [2]
+  uint64_t* w_full = bars + 4;                 // resident weights
+  uint64_t* mma_done = bars + 5;               // final drain of the MMA pipe
+  uint64_t* acc_full = bars + 6;               // [NSLOT]
+  uint64_t* acc_empty = acc_full + p.NSLOT;    // [NSLOT]
+  uint64_t* b_full = acc_empty + p.NSLOT;      // [SB]
+  uint64_t* b_empty = b_full + p.SB;           // [SB]
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   volatile int* abort_flag = &s_abort;
+  const uint32_t tile_cols = (uint32_t)(p.NSLOT * p.Cout);
 
   if (tid == 0) {
     s_abort = 0;
@@ -177,12 +217,12 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
       mbar_init(&a_full[i], kConvThreads);
       mbar_init(&a_empty[i], 1);
     }
-    for (int i = 0; i < kSlots; ++i) {
+    mbar_init(w_full, 1);
+    mbar_init(mma_done, 1);
+    for (int i = 0; i < p.NSLOT; ++i) {
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], kEpiThreads);
     }
-    mbar_init(w_full, 1);
-    mbar_init(mma_done, 1);
     for (int i = 0; i < p.SB; ++i) {
       mbar_init(&b_full[i], 1);
       mbar_init(&b_empty[i], 1);
@@ -197,13 +237,23 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = s_tmem;
-  const int nblocks = 27 * p.KS;
+  if (warp >= kEpiWarp0) {
+    // Every MMA accumulates, so the accumulators start at zero (and the epilogue
+    // zeroes each slot again after reading it).
+    const int grp = (warp - kEpiWarp0) >> 2;
+    const uint32_t lane_base = tmem_base + ((uint32_t)((warp & 3) * 32) << 16);
+    for (uint32_t c = (uint32_t)grp * 16u; c < (uint32_t)T * tile_cols; c += 32u) tmem_zero16(lane_base + c);
+    tmem_wait_st();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
 
   if (warp == 0) {
     // ------------------------------------------------------------ weight producer
     if (lane == 0) {
-      if (p.resident) {
-        const uint32_t total = (uint32_t)nblocks * p.b_block_bytes;
+      if constexpr (RES) {
+        const uint32_t total = (uint32_t)(27 * p.KS) * (p.b_block_bytes / (KDM == 3 ? 3u : 1u));
         mbar_arrive_expect_tx(w_full, total);
         const uint8_t* src = reinterpret_cast<const uint8_t*>(p.wblob);
         for (uint32_t off = 0; off < total;) {
@@ -215,29 +265,27 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
       } else {
         Ring rb;
         uint32_t issued = 0;
+        const uint32_t stage_bytes = (uint32_t)KSS * p.b_block_bytes;
         for (int u = blockIdx.x; u < p.units && !*abort_flag; u += gridDim.x) {
           const Unit un = decode_unit(p, u);
           for (int d = un.od0; d < un.od1 + 2 && !*abort_flag; ++d) {
+            const int kd_hi = min(2, d - un.od0), kd_lo = max(0, d - un.od1 + 1);
             for (int ch = 0; ch < p.nchunks; ++ch) {
-              const int ks_n = chunk_channels(p, ch) >> 3;
-              for (int kd = 2; kd >= 0; --kd) {
-                const int od = d - kd;
-                if (od < un.od0 || od >= un.od1) continue;
+              // The stages in the order the MMA issuer consumes them: KDM 3, the nine
+              // taps (each block holds all three kd); KDM 1, the valid kd from 2 down,
+              // nine taps each.
+              const int nkd = (KDM == 3) ? 1 : kd_hi - kd_lo + 1;
+              for (int k = 0; k < nkd; ++k) {
+                const int tap_base = (KDM == 3) ? 0 : (kd_hi - k) * 9;
                 for (int khw = 0; khw < 9; ++khw) {
-                  // One stage = up to KSS consecutive K-step blocks of this tap (contiguous
-                  // in the blob), fetched with one bulk copy.
-                  for (int s0 = 0; s0 < ks_n; s0 += p.KSS) {
-                    const int nb = min(p.KSS, ks_n - s0);
-                    if (!wait_fast(&b_empty[rb.idx], rb.phase ^ 1u, p.ctl, abort_flag)) goto producer_done;
-                    const int blk = (kd * 9 + khw) * p.KS + ch * (p.CC >> 3) + s0;
-                    const uint32_t bytes = (uint32_t)nb * p.b_block_bytes;
-                    mbar_arrive_expect_tx(&b_full[rb.idx], bytes);
-                    bulk_copy_g2s(smem_b + (size_t)rb.idx * p.KSS * p.b_block_bytes,
-                                  reinterpret_cast<const uint8_t*>(p.wblob) + (size_t)blk * p.b_block_bytes, bytes,
-                                  &b_full[rb.idx]);
-                    rb.next(p.SB);
-                    ++issued;
-                  }
+                  if (!wait_fast(&b_empty[rb.idx], rb.phase ^ 1u, p.ctl, abort_flag)) goto producer_done;
+                  const int blk = (tap_base + khw) * p.KS + ch * KSS;
+                  mbar_arrive_expect_tx(&b_full[rb.idx], stage_bytes);
+                  bulk_copy_g2s(smem_b + (size_t)rb.idx * stage_bytes,
+                                reinterpret_cast<const uint8_t*>(p.wblob) + (size_t)blk * p.b_block_bytes,
+                                stage_bytes, &b_full[rb.idx]);
+                  rb.next((uint32_t)p.SB);
+                  ++issued;
                 }
               }
             }
@@ -264,78 +312,63 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       // Descriptors are formed once and advanced by plain adds in 16-byte units (the
-      // start-address field is the low 14 bits): the issue loop must stay a short
-      // chain of adds for tcgen05.mma to issue at the tensor pipe's rate.
-      const uint32_t idesc_cat = umma_idesc_tf32(128, SCHEME == 0 ? 2 * p.Cout : p.Cout);
-      const uint32_t idesc_one = umma_idesc_tf32(128, p.Cout);
+      // start-address field is the low 14 bits), so the issue loop stays a short
+      // chain of adds and tcgen05.mma.
+      const uint32_t b_rows = (uint32_t)((KDM == 3 ? 6 : 2) * p.Cout);
       const uint64_t a_desc0 = umma_desc_noswizzle(smem_addr(smem_a), (uint32_t)p.NPOS * 16u, 128);
-      const uint64_t b_desc0 = umma_desc_noswizzle(smem_addr(smem_b), (uint32_t)(2 * p.Cout) * 16u, 128);
+      const uint64_t b_desc0 = umma_desc_noswizzle(smem_addr(smem_b), b_rows * 16u, 128);
       const uint32_t a_stage_u = p.a_stage_bytes >> 4, a_half_u = p.a_half_bytes >> 4;
-      const uint32_t ks_u = 2u * (uint32_t)p.NPOS;       // next K-step: two channel groups on
-      const uint32_t b_block_u = p.b_block_bytes >> 4;
-      const uint32_t b_stage_u = b_block_u * (uint32_t)p.KSS;
-      const uint32_t b_lo_u = (uint32_t)p.Cout;           // lo rows start Cout rows further
-      const uint32_t row_u = (uint32_t)p.W;               // one input row (kh step)
-      const uint32_t slot_cols = (uint32_t)(p.T * p.NACC);
-      const uint32_t nacc = (uint32_t)p.NACC;
-      const int CC8 = p.CC >> 3;
+      const uint32_t ks_u = 2u * (uint32_t)p.NPOS;  // next K-step: two channel groups on
+      const uint32_t blk_u = p.b_block_bytes >> 4;
+      const uint32_t lo_u = b_rows >> 1;             // lo rows follow the hi rows
+      const uint32_t row_u = (uint32_t)p.W;          // one input row (kh step)
+      const uint32_t cout = (uint32_t)p.Cout;
+      const uint32_t idesc1 = umma_idesc_tf32(128, p.Cout);
       bool ok = true;
-      if (p.resident) ok = mbar_wait_bounded(w_full, 0, p.ctl, abort_flag);
+      if constexpr (RES) ok = mbar_wait_bounded(w_full, 0, p.ctl, abort_flag);
       Ring ra, rb;
+      uint32_t empty_par = 0;  // per slot: uses so far, mod 2
       uint32_t plane_seq = 0;
       for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
         const Unit un = decode_unit(p, u);
+        const uint32_t s0 = unit_slot0(p, plane_seq);
         for (int d = un.od0; ok && d < un.od1 + 2; ++d) {
+          // Output planes fed by input plane d: od = d - kd for kd in [kd_lo, kd_hi].
+          const int kd_hi = min(2, d - un.od0), kd_lo = max(0, d - un.od1 + 1);
           for (int ch = 0; ok && ch < p.nchunks; ++ch) {
-            const int ks_n = chunk_channels(p, ch) >> 3;
             if (!(ok = wait_fast(&a_full[ra.idx], ra.phase, p.ctl, abort_flag))) break;
             tc_fence_after();
+            if (ch == 0 && kd_lo == 0) {
+              // Plane d opens output plane od = d: its slot must have been drained.
+              const uint32_t s = slot_add(p, s0, d - un.od0);
+              if (!(ok = wait_fast(&acc_empty[s], ((empty_par >> s) & 1u) ^ 1u, p.ctl, abort_flag))) break;
+              empty_par ^= 1u << s;
+              tc_fence_after();
+            }
             const uint64_t ah0 = a_desc0 + (uint64_t)(ra.idx * a_stage_u);
             const uint64_t al0 = ah0 + a_half_u;
-            for (int kd = 2; ok && kd >= 0; --kd) {
-              const int od = d - kd;
-              if (od < un.od0 || od >= un.od1) continue;
-              const uint32_t pseq = plane_seq + (uint32_t)(od - un.od0);
-              const uint32_t slot = pseq & (kSlots - 1);
-              if (kd == 0 && ch == 0) {
-                if (!(ok = wait_fast(&acc_empty[slot], ((pseq >> 2) & 1u) ^ 1u, p.ctl, abort_flag))) break;
-                tc_fence_after();
+            if constexpr (KDM == 3) {
+              // One window: the accumulators of od = d - kd_hi .. d - kd_lo are adjacent
+              // (slots ascend with od), the B rows of kd = kd_hi .. kd_lo too.
+              const uint32_t nkd = (uint32_t)(kd_hi - kd_lo + 1);
+              const uint32_t dcol = tmem_base + (s0 + (uint32_t)(d - kd_hi - un.od0)) * cout;
+              const uint32_t idesc = umma_idesc_tf32(128, (int)(nkd * cout));
+              const uint64_t bwin = b_desc0 + (uint64_t)((uint32_t)(2 - kd_hi) * cout);
+              ok = issue_taps<T, KSS, RES>(p, dcol, tile_cols, ah0, al0, bwin, lo_u, ks_u, blk_u, row_u, idesc, 0,
+                                           ch * KSS, b_full, b_empty, rb, abort_flag);
+            } else {
+              for (int kd = kd_hi; ok && kd >= kd_lo; --kd) {
+                const uint32_t dcol = tmem_base + slot_add(p, s0, d - kd - un.od0) * cout;
+                ok = issue_taps<T, KSS, RES>(p, dcol, tile_cols, ah0, al0, b_desc0, lo_u, ks_u, blk_u, row_u,
+                                             idesc1, kd * 9, ch * KSS, b_full, b_empty, rb, abort_flag);
+                if (ok && kd == 2 && ch == p.nchunks - 1) umma_commit(&acc_full[slot_add(p, s0, d - 2 - un.od0)]);
               }
-              const uint32_t d0 = tmem_base + slot * slot_cols;
-              // The first MMA of a plane (kd = 0, first chunk, first tap, first K-step)
-              // overwrites the accumulator; every later one adds to it.
-              uint32_t acc = (kd == 0 && ch == 0) ? 0u : 1u;
-#pragma unroll
-              for (int kh = 0; kh < 3; ++kh) {
-#pragma unroll
-                for (int kw = 0; kw < 3; ++kw) {
-                  const uint32_t tap_u = (uint32_t)kh * row_u + (uint32_t)kw;
-                  const int tap = (kd * 3 + kh) * 3 + kw;
-                  for (int s0 = 0; s0 < ks_n; s0 += KSS) {
-                    uint64_t bst;
-                    if (p.resident) {
-                      bst = b_desc0 + (uint64_t)((uint32_t)(tap * p.KS + ch * CC8 + s0) * b_block_u);
-                    } else {
-                      if (!(ok = wait_fast(&b_full[rb.idx], rb.phase, p.ctl, abort_flag))) break;
-                      tc_fence_after();
-                      bst = b_desc0 + (uint64_t)(rb.idx * b_stage_u);
-                    }
-                    issue_stage<SCHEME, T, KSS>(d0, ah0, al0, bst, (uint32_t)s0 * ks_u + tap_u, ks_u, b_block_u,
-                                                b_lo_u, nacc, idesc_cat, idesc_one, acc);
-                    if (!p.resident) {
-                      umma_commit(&b_empty[rb.idx]);
-                      rb.next(p.SB);
-                    }
-                  }
-                  if (!ok) break;
-                }
-                if (!ok) break;
-              }
-              if (ok && kd == 2 && ch == p.nchunks - 1) umma_commit(&acc_full[slot]);
             }
             umma_commit(&a_empty[ra.idx]);
             ra.next(kAStages);
           }
+          // KDM 3: output plane d - 2 received its last contribution with this plane.
+          if (KDM == 3 && ok && kd_hi == 2) umma_commit(&acc_full[s0 + (uint32_t)(d - 2 - un.od0)]);
         }
         plane_seq += (uint32_t)(un.od1 - un.od0);
       }
@@ -349,16 +382,16 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
     const int ct = tid - kConvWarp0 * 32;
     const size_t HW = (size_t)p.H * p.W;
     const int plane_pos = p.H * p.W;
+    const int CC = KSS * 8;
     Ring ra;
     for (int u = blockIdx.x; u < p.units && !*abort_flag; u += gridDim.x) {
       const Unit un = decode_unit(p, u);
-      const int p0 = un.g * p.T * 128;
+      const int p0 = un.g * T * 128;
       for (int d = un.od0; d < un.od1 + 2; ++d) {
         for (int ch = 0; ch < p.nchunks; ++ch) {
           if (!warp_wait(&a_empty[ra.idx], ra.phase ^ 1u, p.ctl, abort_flag)) goto convert_done;
-          const int c0 = ch * p.CC;
-          const int groups = chunk_channels(p, ch) >> 2;
-          const int items = groups * p.NPOS;
+          const int c0 = ch * CC;
+          const int items = (CC / 4) * p.NPOS;
           const uint32_t hi_base = smem_addr(smem_a) + ra.idx * p.a_stage_bytes;
           const uint32_t lo_base = hi_base + p.a_half_bytes;
           const float* xplane = p.x + ((size_t)un.n * p.Cin) * p.D * HW + (size_t)d * HW;
@@ -381,8 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
             for (int k = 0; k < 2; ++k) {
               const int i = i0 + k * kConvThreads;
               if (i < items) {
-                const int grp = i / p.NPOS, pp = i - grp * p.NPOS;
-                const uint32_t off = (uint32_t)(grp * p.NPOS + pp) * 16u;
+                const uint32_t off = (uint32_t)i * 16u;  // [group][position][4]
                 float h[4], l[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) split_tf32(v[k][j], h[j], l[j]);
@@ -408,21 +440,23 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
     const size_t OHW = (size_t)p.OH * p.OW;
     const int PH = p.OH / 2, PW = p.OW / 2;
     const int cchunks = p.Cout >> 4;
-    const int items = p.T * cchunks;
+    const int items = T * cchunks;
     float* s_x = s_epi + grp * (16 * 32);          // pool: h-pair exchange [16][32] per group
     float* s_prev = s_epi + 2 * (16 * 32);         // pool: even-plane maxima [T][Cout][32]
+    const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
+    uint32_t full_par = 0;  // per slot: completions seen so far, mod 2
     uint32_t plane_seq = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
       const Unit un = decode_unit(p, u);
-      const int p0 = un.g * p.T * 128;
+      const uint32_t s0 = unit_slot0(p, plane_seq);
+      const int p0 = un.g * T * 128;
       float psum = 0.0f;
       for (int od = un.od0; od < un.od1; ++od) {
-        const uint32_t pseq = plane_seq + (uint32_t)(od - un.od0);
-        const uint32_t slot = pseq & (kSlots - 1);
-        if (!(ok = warp_wait(&acc_full[slot], (pseq >> 2) & 1u, p.ctl, abort_flag))) break;
+        const uint32_t slot = slot_add(p, s0, od - un.od0);
+        if (!(ok = warp_wait(&acc_full[slot], (full_par >> slot) & 1u, p.ctl, abort_flag))) break;
+        full_par ^= 1u << slot;
         tc_fence_after();
-        const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16) + slot * (uint32_t)(p.T * p.NACC);
         const bool pool_plane = (EPI == IG3_EPI_POOL_REDUCE) && (od / 2 < p.OD / 2);
         for (int it = grp; it < items; it += 2) {
           const int t = it / cchunks;
@@ -431,18 +465,11 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
           const int pos = p0 + lp;
           const int oh = pos / p.W, ow = pos - oh * p.W;
           const bool valid = (oh < p.OH) && (ow < p.OW);
-          const uint32_t tcol = lane_base + (uint32_t)(t * p.NACC);
+          const uint32_t taddr = lane_base + (uint32_t)t * tile_cols + slot * (uint32_t)p.Cout + (uint32_t)c0;
           float v[16];
-          tmem_ld16(tcol + c0, v);
-          if constexpr (SCHEME == 0) {
-            float w2[16];
-            tmem_ld16(tcol + p.Cout + c0, w2);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] += w2[j];
-          } else {
-            tmem_wait_ld();
-          }
+          tmem_ld16(taddr, v);
+          tmem_wait_ld();
+          tmem_zero16(taddr);  // ready for the slot's next use
           if constexpr (EPI != IG3_EPI_POOL_REDUCE) {
             float* yb = p.y + (((size_t)un.n * p.Cout + c0) * p.OD + od) * OHW + (size_t)oh * p.OW + ow;
 #pragma unroll
@@ -491,6 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
             }
           }
         }
+        tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&acc_empty[slot]);
       }
@@ -520,9 +548,17 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
   }
 }
 
+// Kernel variants: (KDM, T, KSS, resident).  The planner only produces these.
+struct Variant {
+  int kdm, t, kss, res;
+};
+constexpr Variant kVariants[] = {
+    {3, 1, 2, 0}, {3, 2, 2, 0},                                                // streaming, one window per MMA
+    {3, 1, 1, 1}, {3, 1, 2, 1}, {3, 2, 1, 1}, {3, 2, 2, 1}, {3, 4, 1, 1}, {3, 4, 2, 1},  // resident
+    {1, 1, 2, 0}, {1, 1, 1, 0},                                                // streaming, one kd per MMA
+};
 
-// Launches the kernel variant matching p.scheme, p.T and p.KSS (the planner only
-// produces the combinations listed here).  Returns an ig3 status.
+// Launches the kernel variant matching p (KDM, T, KSS, resident).  Returns an ig3 status.
 template <int EPI>
 int launch_kernel(const TcParams& p, size_t smem, int grid, cudaStream_t stream) {
   auto go = [&](auto kernel) -> int {
@@ -531,21 +567,21 @@ int launch_kernel(const TcParams& p, size_t smem, int grid, cudaStream_t stream)
     kernel<<<grid, kThreads, smem, stream>>>(p);
     return count_launch(cuda_status(cudaGetLastError(), "conv3d TC kernel launch"));
   };
-  const int key = p.scheme * 100 + p.T * 10 + p.KSS;
+  const int key = p.KDM * 1000 + p.T * 100 + p.KSS * 10 + p.resident;
   switch (key) {
-    case 11: return go(conv3d_tc_kernel<EPI, 0, 1, 1>);
-    case 12: return go(conv3d_tc_kernel<EPI, 0, 1, 2>);
-    case 14: return go(conv3d_tc_kernel<EPI, 0, 1, 4>);
-    case 21: return go(conv3d_tc_kernel<EPI, 0, 2, 1>);
-    case 22: return go(conv3d_tc_kernel<EPI, 0, 2, 2>);
-    case 24: return go(conv3d_tc_kernel<EPI, 0, 2, 4>);
-    case 41: return go(conv3d_tc_kernel<EPI, 0, 4, 1>);
-    case 42: return go(conv3d_tc_kernel<EPI, 0, 4, 2>);
-    case 44: return go(conv3d_tc_kernel<EPI, 0, 4, 4>);
-    case 111: return go(conv3d_tc_kernel<EPI, 1, 1, 1>);
-    case 112: return go(conv3d_tc_kernel<EPI, 1, 1, 2>);
-    default: return fail(IG3_ERR_UNSUPPORTED, "conv3d TC: no kernel variant for scheme %d, T %d, %d K-steps per stage",
-                         p.scheme, p.T, p.KSS);
+    case 3120: return go(conv3d_tc_kernel<EPI, 3, 1, 2, false>);
+    case 3220: return go(conv3d_tc_kernel<EPI, 3, 2, 2, false>);
+    case 3111: return go(conv3d_tc_kernel<EPI, 3, 1, 1, true>);
+    case 3121: return go(conv3d_tc_kernel<EPI, 3, 1, 2, true>);
+    case 3211: return go(conv3d_tc_kernel<EPI, 3, 2, 1, true>);
+    case 3221: return go(conv3d_tc_kernel<EPI, 3, 2, 2, true>);
+    case 3411: return go(conv3d_tc_kernel<EPI, 3, 4, 1, true>);
+    case 3421: return go(conv3d_tc_kernel<EPI, 3, 4, 2, true>);
+    case 1120: return go(conv3d_tc_kernel<EPI, 1, 1, 2, false>);
+    case 1110: return go(conv3d_tc_kernel<EPI, 1, 1, 1, false>);
+    default:
+      return fail(IG3_ERR_UNSUPPORTED, "conv3d TC: no kernel variant for KDM %d, T %d, %d K-steps, resident %d",
+                  p.KDM, p.T, p.KSS, p.resident);
   }
 }
 

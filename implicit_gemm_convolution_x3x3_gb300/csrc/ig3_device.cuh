@@ -176,6 +176,19 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// Zero 32 lanes x 16 consecutive columns (the lanes of this warp's quadrant, as for
+// tmem_ld16).  Follow with tmem_wait_st() before signalling that the columns are free.
+__device__ __forceinline__ void tmem_zero16(uint32_t taddr) {
+  const uint32_t z = 0u;
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, "
+      "%1};" ::"r"(taddr),
+      "r"(z)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // Split x into hi + lo with hi exactly representable in tf32 (low 13 mantissa bits
 // cleared) and lo = x - hi computed exactly.  The tensor core truncates tf32
 // operands, so hi is used exactly and hi*b_hi + hi*b_lo + lo*b_hi carries the
