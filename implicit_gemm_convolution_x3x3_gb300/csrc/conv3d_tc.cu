@@ -300,6 +300,7 @@ int conv3d_tc_launch(const Conv3dArgs& a) {
   p.y = a.y;
   p.partial = reinterpret_cast<float*>(ws + pl.blob_bytes);
   p.inv_div = (a.epi == IG3_EPI_POOL_REDUCE) ? 1.0f / a.divisor : 1.0f;
+  p.vec = ((size_t)a.H * a.W % 4 == 0 && reinterpret_cast<uintptr_t>(a.x) % 16 == 0) ? 1 : 0;
   p.ctl = wait_ctl();
   if (!p.ctl.status) return fail(IG3_ERR_CUDA, "conv3d TC path: device status word unavailable");
 

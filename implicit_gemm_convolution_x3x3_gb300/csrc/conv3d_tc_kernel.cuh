@@ -39,6 +39,7 @@ struct TcParams {
   int resident;  // weights loaded once
   int SB;        // weight ring stages (streaming)
   int epi;
+  int vec;       // x planes 16-byte aligned with H*W % 4 == 0: convert with 16-byte loads
   float inv_div;
   uint32_t a_half_bytes;   // one of hi / lo in an A stage
   uint32_t a_stage_bytes;  // hi + lo
@@ -178,6 +179,18 @@ static __device__ __forceinline__ bool issue_taps(const TcParams& p, uint32_t dc
   return good;
 }
 
+// 16 consecutive floats from shared memory (16-byte aligned), the same for every lane.
+static __device__ __forceinline__ void load_bias16(const float* src, float (&v)[16]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 q = reinterpret_cast<const float4*>(src)[i];
+    v[4 * i] = q.x;
+    v[4 * i + 1] = q.y;
+    v[4 * i + 2] = q.z;
+    v[4 * i + 3] = q.w;
+  }
+}
+
 static __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
@@ -192,6 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ float s_red[kEpiThreads / 32];
+  __shared__ __align__(16) float s_bias[128];
 
   uint8_t* smem_a = smem;
   uint8_t* smem_b = smem + p.off_b;
@@ -211,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
   volatile int* abort_flag = &s_abort;
   const uint32_t tile_cols = (uint32_t)(p.NSLOT * p.Cout);
 
+  if (tid < p.Cout) s_bias[tid] = p.bias ? p.bias[tid] : 0.0f;
   if (tid == 0) {
     s_abort = 0;
     for (int i = 0; i < kAStages; ++i) {
@@ -238,11 +253,15 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
   tc_fence_after();
   const uint32_t tmem_base = s_tmem;
   if (warp >= kEpiWarp0) {
-    // Every MMA accumulates, so the accumulators start at zero (and the epilogue
-    // zeroes each slot again after reading it).
+    // Every MMA accumulates, so each accumulator starts as the conv bias of its
+    // column's channel (and the epilogue writes the bias back after reading a slot).
     const int grp = (warp - kEpiWarp0) >> 2;
     const uint32_t lane_base = tmem_base + ((uint32_t)((warp & 3) * 32) << 16);
-    for (uint32_t c = (uint32_t)grp * 16u; c < (uint32_t)T * tile_cols; c += 32u) tmem_zero16(lane_base + c);
+    for (uint32_t c = (uint32_t)grp * 16u; c < (uint32_t)T * tile_cols; c += 32u) {
+      float bv[16];
+      load_bias16(s_bias + c % (uint32_t)p.Cout, bv);
+      tmem_st16(lane_base + c, bv);
+    }
     tmem_wait_st();
   }
   tc_fence_before();
@@ -395,6 +414,51 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
           const uint32_t hi_base = smem_addr(smem_a) + ra.idx * p.a_stage_bytes;
           const uint32_t lo_base = hi_base + p.a_half_bytes;
           const float* xplane = p.x + ((size_t)un.n * p.Cin) * p.D * HW + (size_t)d * HW;
+          if (p.vec) {
+            // Item = (channel group, 4 consecutive positions): four 16-byte loads (one
+            // per channel, coalesced along positions), transposed in registers to four
+            // [position][4 channels] entries.  H*W % 4 == 0, so a quad lies wholly inside
+            // or wholly past the plane.
+            const int quads = p.NPOS >> 2;
+            const int vitems = (CC / 4) * quads;
+            for (int i0 = ct; i0 < vitems; i0 += 2 * kConvThreads) {
+              float4 v[2][4];
+#pragma unroll
+              for (int k = 0; k < 2; ++k) {
+                const int i = i0 + k * kConvThreads;
+                const int grp = i / quads, qd = i - grp * quads;
+                const int pos = p0 + 4 * qd;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  const int c = c0 + grp * 4 + j;
+                  v[k][j] = (i < vitems && pos < plane_pos && c < p.Cin)
+                                ? __ldg(reinterpret_cast<const float4*>(xplane + (size_t)c * p.D * HW + pos))
+                                : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                }
+              }
+#pragma unroll
+              for (int k = 0; k < 2; ++k) {
+                const int i = i0 + k * kConvThreads;
+                if (i < vitems) {
+                  const int grp = i / quads, qd = i - grp * quads;
+                  const uint32_t off = (uint32_t)(grp * p.NPOS + 4 * qd) * 16u;
+                  float h[4][4], l[4][4];
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) {
+                    split_tf32(v[k][j].x, h[0][j], l[0][j]);
+                    split_tf32(v[k][j].y, h[1][j], l[1][j]);
+                    split_tf32(v[k][j].z, h[2][j], l[2][j]);
+                    split_tf32(v[k][j].w, h[3][j], l[3][j]);
+                  }
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    st_shared_v4(hi_base + off + 16u * e, h[e][0], h[e][1], h[e][2], h[e][3]);
+                    st_shared_v4(lo_base + off + 16u * e, l[e][0], l[e][1], l[e][2], l[e][3]);
+                  }
+                }
+              }
+            }
+          } else
           for (int i0 = ct; i0 < items; i0 += 2 * kConvThreads) {
             float v[2][4];
 #pragma unroll
@@ -466,15 +530,16 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
           const int oh = pos / p.W, ow = pos - oh * p.W;
           const bool valid = (oh < p.OH) && (ow < p.OW);
           const uint32_t taddr = lane_base + (uint32_t)t * tile_cols + slot * (uint32_t)p.Cout + (uint32_t)c0;
-          float v[16];
+          float v[16], bv[16];
           tmem_ld16(taddr, v);
+          load_bias16(s_bias + c0, bv);
           tmem_wait_ld();
-          tmem_zero16(taddr);  // ready for the slot's next use
+          tmem_st16(taddr, bv);  // the slot's next use starts from the bias again
           if constexpr (EPI != IG3_EPI_POOL_REDUCE) {
             float* yb = p.y + (((size_t)un.n * p.Cout + c0) * p.OD + od) * OHW + (size_t)oh * p.OW + ow;
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              float val = v[j] + (p.bias ? __ldg(&p.bias[c0 + j]) : 0.0f);
+              float val = v[j];
               if (EPI == IG3_EPI_TANH_MISH) val = tanh_mish(val);
               if (valid) yb[(size_t)j * p.OD * OHW] = val;
             }
@@ -488,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
             float hm[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              const float z = (v[j] + (p.bias ? __ldg(&p.bias[c0 + j]) : 0.0f)) * p.inv_div;
+              const float z = v[j] * p.inv_div;
               hm[j] = fmaxf(z, __shfl_xor_sync(0xffffffffu, z, 1));
             }
             if (p.W <= 16) {

@@ -176,14 +176,15 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// Zero 32 lanes x 16 consecutive columns (the lanes of this warp's quadrant, as for
-// tmem_ld16).  Follow with tmem_wait_st() before signalling that the columns are free.
-__device__ __forceinline__ void tmem_zero16(uint32_t taddr) {
-  const uint32_t z = 0u;
+// Store 16 consecutive columns for the 32 lanes of this warp's quadrant (thread i of
+// the warp writes lane 32 * (warp % 4) + i).  Follow with tmem_wait_st() before
+// signalling that the columns are written.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, "
-      "%1};" ::"r"(taddr),
-      "r"(z)
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "f"(v[8]), "f"(v[9]),
+      "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15])
       : "memory");
 }
 
@@ -201,18 +202,20 @@ __device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
 // ------------------------------------------------------------------ activation
 // tanh(z) = 1 - 2 / (e^(2z) + 1), from the definition.  Absolute error a few
 // float ulps of 1 for all z (the form is not meant for relative accuracy near 0);
-// e^(2z) overflowing to +inf gives 1, underflowing to 0 gives -1.
+// e^(2z) overflowing to +inf gives 1 (the fast division by inf yields 0),
+// underflowing to 0 gives -1.
 __device__ __forceinline__ float tanh_from_exp(float z) {
-  return 1.0f - 2.0f / (__expf(2.0f * z) + 1.0f);
+  return 1.0f - __fdividef(2.0f, __expf(2.0f * z) + 1.0f);
 }
 
 // tanh(mish(y)), mish(y) = y * tanh(softplus(y)).  With n = e^y,
 // tanh(log(1 + n)) = ((1+n)^2 - 1) / ((1+n)^2 + 1) = n(n+2) / (n(n+2) + 2),
-// so one exponential replaces exp + log1p + tanh.  For y > 15, tanh(softplus(y))
-// differs from 1 by about 2e-13, below float resolution, so mish(y) = y.
+// so one exponential replaces exp + log1p + tanh.  For y >= 15, tanh(softplus(y))
+// differs from 1 by about 2e-13, below float resolution, and with n = e^15 the ratio
+// already rounds to 1: clamping the exponent at 15 gives mish(y) = y there without a
+// branch (and keeps n(n+2) finite).  Two exponentials and two fast reciprocals.
 __device__ __forceinline__ float tanh_mish(float y) {
-  if (y > 15.0f) return tanh_from_exp(y);
-  const float n = __expf(y);
+  const float n = __expf(fminf(y, 15.0f));
   const float t = n * (n + 2.0f);
   return tanh_from_exp(y * __fdividef(t, t + 2.0f));
 }
