@@ -75,14 +75,21 @@ using namespace tc;
 // Weights [Cout][Cin][27] -> pre-split K-step blocks, each [khalf][rows][4] (rows
 // of 4 consecutive channels, the two channel halves of the K-step one after the
 // other), channels past Cin zero:
-//   KDM 3: block (khw * KS + ks), rows [hi kd=2 | hi kd=1 | hi kd=0 | lo kd=2 | lo kd=1 |
-//          lo kd=0] x Cout, so any run of adjacent kd is a contiguous row range;
-//   KDM 1: block ((kd * 9 + khw) * KS + ks), rows [hi | lo] x Cout.
-// khw = kh * 3 + kw.  Both layouts hold 27 * KS * 2 * 2*Cout * 4 floats.
+//   KDM 3:       block (khw * KS + ks), rows [hi kd=2 | hi kd=1 | hi kd=0 | lo kd=2 |
+//                lo kd=1 | lo kd=0] x Cout, so any run of adjacent kd is a contiguous
+//                row range;
+//   KDM 3, HL:   block (khw * KS + ks), rows [hi kd=2 | lo kd=2 | hi kd=1 | lo kd=1 |
+//                hi kd=0 | lo kd=0 | hi kd=2 | 0 | hi kd=1 | 0 | hi kd=0 | 0] x Cout;
+//   KDM 1:       block ((kd * 9 + khw) * KS + ks), rows [hi | lo] x Cout.
+// khw = kh * 3 + kw.
+__host__ __device__ int blob_rows(int kdm, int hl, int Cout) { return (kdm == 3 ? (hl ? 12 : 6) : 2) * Cout; }
+size_t blob_floats(int kdm, int hl, int KS, int Cout) {
+  return (size_t)(kdm == 3 ? 9 : 27) * KS * 2 * blob_rows(kdm, hl, Cout) * 4;
+}
+
 __global__ void conv3d_tc_prep_weights(const float* __restrict__ w, float* __restrict__ blob, int Cin, int Cout,
-                                       int KS, int kdm) {
-  const int rows = (kdm == 3 ? 6 : 2) * Cout;
-  const int total = 27 * KS * 2 * (2 * Cout) * 4;
+                                       int KS, int kdm, int hl, int total) {
+  const int rows = blob_rows(kdm, hl, Cout);
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
     const int j = i & 3;
     int r = i >> 2;
@@ -93,8 +100,16 @@ __global__ void conv3d_tc_prep_weights(const float* __restrict__ w, float* __res
     const int ks = r % KS;
     const int blk = r / KS;
     int tap, co;
-    bool hi;
-    if (kdm == 3) {
+    bool hi, zero = false;
+    if (kdm == 3 && hl) {
+      const int half = row / (6 * Cout);  // 0: [hi | lo] per kd, 1: [hi | 0] per kd
+      const int rr = row % (6 * Cout);
+      const int kd = 2 - rr / (2 * Cout);
+      hi = (rr % (2 * Cout)) < Cout;
+      zero = (half == 1) && !hi;
+      co = rr % Cout;
+      tap = kd * 9 + blk;  // blk = khw
+    } else if (kdm == 3) {
       hi = row < 3 * Cout;
       const int rr = hi ? row : row - 3 * Cout;
       const int kd = 2 - rr / Cout;
@@ -109,7 +124,7 @@ __global__ void conv3d_tc_prep_weights(const float* __restrict__ w, float* __res
     const float v = (c < Cin) ? w[((size_t)co * Cin + c) * 27 + tap] : 0.0f;
     float h, l;
     split_tf32(v, h, l);
-    blob[i] = hi ? h : l;
+    blob[i] = zero ? 0.0f : (hi ? h : l);
   }
 }
 
@@ -125,24 +140,25 @@ struct Plan {
 int positions_tiles(int OH, int W, int T) { return ((OH * W) + T * 128 - 1) / (T * 128); }
 
 // Cycle estimate of one input plane's MMAs (per SM): nkd output planes fed, per
-// (tap, K-step, tile) three MMAs.  A tcgen05.mma takes ~46 cycles to issue from one
-// thread and N/2 cycles to execute (M = 128, K = 8, N >= 96); every streamed weight
-// stage adds ~250 cycles of wait and commit to the issuing thread.
-double plane_cycles(int kdm, int nkd, int Cout, int KS, int nchunks, int T, bool res) {
+// (tap, K-step, tile) three MMAs (two with HL).  A tcgen05.mma takes ~46 cycles to
+// issue from one thread (small-N MMAs measure nearer 70) and N/2 cycles to execute
+// (M = 128, K = 8); every streamed weight stage adds ~250 cycles of wait and commit to
+// the issuing thread.
+double plane_cycles(int kdm, int hl, int nkd, int Cout, int KS, int nchunks, int T, bool res) {
   const double issue_one = 46.0;
-  const int mmas_per_step = (kdm == 3) ? 3 : 3 * nkd;
-  const int n = (kdm == 3) ? nkd * Cout : Cout;
+  const int mmas_per_step = (kdm == 3) ? (hl ? 2 : 3) : 3 * nkd;
+  const int n = (kdm == 3) ? nkd * Cout * (hl ? 2 : 1) : Cout;
   const double exec = 9.0 * KS * T * mmas_per_step * std::max(issue_one, 0.5 * n);
   const double stages = res ? 0.0 : 9.0 * nchunks * (kdm == 3 ? 1 : nkd);
   const double issue = 9.0 * KS * T * mmas_per_step * issue_one + 250.0 * stages;
   return std::max(exec, issue) + 300.0 * nchunks;  // A hand-over per chunk
 }
 
-double unit_cycles(int kdm, int planes, int Cout, int KS, int nchunks, int T, bool res) {
+double unit_cycles(int kdm, int hl, int planes, int Cout, int KS, int nchunks, int T, bool res) {
   double c = 0.0;
   for (int d = 0; d < planes + 2; ++d) {
     const int kd_hi = std::min(2, d), kd_lo = std::max(0, d - planes + 1);
-    c += plane_cycles(kdm, kd_hi - kd_lo + 1, Cout, KS, nchunks, T, res);
+    c += plane_cycles(kdm, hl, kd_hi - kd_lo + 1, Cout, KS, nchunks, T, res);
   }
   return c;
 }
@@ -163,22 +179,23 @@ Plan make_plan_uncached(int N, int Cin, int D, int H, int W, int Cout, int epi, 
   }
   const int OD = D - 2, OH = H - 2;
   const int kdm = (3 * Cout <= 256) ? 3 : 1;
+  const int hl = (kdm == 3 && 6 * Cout <= 256) ? 1 : 0;
   const int ks0 = (Cin + 7) / 8;
   const int step = (epi == IG3_EPI_POOL_REDUCE) ? 2 : 1;
   double best = 1e300;
   for (const Variant& v : kVariants) {
-    if (v.kdm != kdm) continue;
+    if (v.kdm != kdm || v.hl != hl) continue;
     const int T = v.t, kss = v.kss;
     const bool res = v.res != 0;
     const int KS = (ks0 + kss - 1) / kss * kss;
     const int nchunks = KS / kss;
-    const int nslot = std::min(kMaxSlots, kTmemCols / (T * Cout));
+    const int nslot = std::min(kMaxSlots, kTmemCols / (T * Cout * (hl ? 2 : 1)));
     if (nslot < (kdm == 3 ? step : 4)) continue;
     const int npos = ((T * 128 + 2 * W + 2) + 7) / 8 * 8;
     const uint32_t a_half = (uint32_t)(2 * kss) * npos * 16u;
     const uint32_t a_stage = 2 * a_half;
-    const uint32_t blk = (uint32_t)((kdm == 3 ? 192 : 64) * Cout);
-    const uint32_t blob = (uint32_t)(1728 * KS * Cout);
+    const uint32_t blk = (uint32_t)(2 * blob_rows(kdm, hl, Cout) * 16);
+    const uint32_t blob = (uint32_t)(blob_floats(kdm, hl, KS, Cout) * 4);
     const uint32_t epi_bytes = (epi == IG3_EPI_POOL_REDUCE) ? (uint32_t)(2 * 16 * 32 + T * Cout * 32) * 4u : 0u;
     const uint32_t off_b = kAStages * a_stage;
     // 2 KB for static shared memory and alignment; barriers for the largest ring.
@@ -200,8 +217,8 @@ Plan make_plan_uncached(int N, int Cin, int D, int H, int W, int Cout, int epi, 
       const int last = OD - (S - 1) * P;
       const long long units = (long long)N * G * S;
       const int grid = (int)std::min<long long>(units, sms);
-      const double c_full = unit_cycles(kdm, P, Cout, KS, nchunks, T, res);
-      const double c_last = unit_cycles(kdm, last, Cout, KS, nchunks, T, res);
+      const double c_full = unit_cycles(kdm, hl, P, Cout, KS, nchunks, T, res);
+      const double c_last = unit_cycles(kdm, hl, last, Cout, KS, nchunks, T, res);
       // Round-robin over the grid: CTA c takes units c, c + grid, ...; a unit is
       // the last split iff u % S == S - 1.
       double worst = 0.0;
@@ -223,6 +240,7 @@ Plan make_plan_uncached(int N, int Cin, int D, int H, int W, int Cout, int epi, 
         p.T = T;
         p.NPOS = npos;
         p.KDM = kdm;
+        p.HL = hl;
         p.NSLOT = nslot;
         p.G = G;
         p.S = S;
@@ -233,6 +251,7 @@ Plan make_plan_uncached(int N, int Cin, int D, int H, int W, int Cout, int epi, 
         p.a_half_bytes = a_half;
         p.a_stage_bytes = a_stage;
         p.b_block_bytes = blk;
+        p.blob_bytes = blob;
         p.off_b = off_b;
         p.off_epi = off_b + (res ? blob : (uint32_t)sb * kss * blk);
         p.off_bar = (p.off_epi + epi_bytes + 127) / 128 * 128;
@@ -247,7 +266,7 @@ Plan make_plan_uncached(int N, int Cin, int D, int H, int W, int Cout, int epi, 
   }
   // Sizes that do not depend on the plan (nor on the device): the blob padded to a
   // multiple of 4 K-steps, partials for the finest possible split.
-  pl.blob_bytes = align_up((size_t)1728 * ((ks0 + 3) / 4 * 4) * Cout, 256);
+  pl.blob_bytes = align_up(blob_floats(kdm, hl, (ks0 + 3) / 4 * 4, Cout) * 4, 256);
   pl.partial_bytes =
       (epi == IG3_EPI_POOL_REDUCE) ? align_up((size_t)N * positions_tiles(OH, W, 1) * OD * sizeof(float), 256) : 0;
   return pl;
@@ -304,9 +323,9 @@ int conv3d_tc_launch(const Conv3dArgs& a) {
   p.ctl = wait_ctl();
   if (!p.ctl.status) return fail(IG3_ERR_CUDA, "conv3d TC path: device status word unavailable");
 
-  const int total = 27 * p.KS * 2 * (2 * p.Cout) * 4;
+  const int total = (int)blob_floats(p.KDM, p.HL, p.KS, p.Cout);
   conv3d_tc_prep_weights<<<std::min((total + 255) / 256, 4 * sms), 256, 0, a.stream>>>(
-      a.w, const_cast<float*>(p.wblob), a.Cin, a.Cout, p.KS, p.KDM);
+      a.w, const_cast<float*>(p.wblob), a.Cin, a.Cout, p.KS, p.KDM, p.HL, total);
   int st = count_launch(cuda_status(cudaGetLastError(), "conv3d TC weight prep launch"));
   if (st != IG3_OK) return st;
 

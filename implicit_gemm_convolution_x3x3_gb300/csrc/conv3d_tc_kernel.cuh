@@ -33,7 +33,8 @@ struct TcParams {
   int T;         // position tiles of 128 per unit
   int NPOS;      // positions held per A stage
   int KDM;       // 3: one MMA spans the kd = 2, 1, 0 accumulators; 1: one MMA per kd
-  int NSLOT;     // accumulator slots per tile, Cout columns each
+  int HL;        // KDM 3 only: hi and lo products in separate columns (slot = 2*Cout)
+  int NSLOT;     // accumulator slots per tile, Cout (HL: 2*Cout) columns each
   int G, S, P;   // tile groups per plane, plane splits, output planes per split
   int units;
   int resident;  // weights loaded once
@@ -44,6 +45,7 @@ struct TcParams {
   uint32_t a_half_bytes;   // one of hi / lo in an A stage
   uint32_t a_stage_bytes;  // hi + lo
   uint32_t b_block_bytes;  // one K-step block of B
+  uint32_t blob_bytes;     // all blocks (resident weights)
   uint32_t off_b, off_epi, off_bar;  // shared-memory offsets
   WaitCtl ctl;
 };
@@ -117,14 +119,17 @@ static __device__ __forceinline__ bool wait_fast(uint64_t* bar, uint32_t parity,
 }
 
 // The MMAs of one weight stage (KSS K-steps x T position tiles), fully unrolled so
-// the issue is a straight run of adds and tcgen05.mma.  Each product of the split
-// (A_hi B_hi, A_hi B_lo, A_lo B_hi) is one MMA into the same accumulator columns;
-// the accumulators start at zero, so every MMA accumulates.
+// the issue is a straight run of adds and tcgen05.mma.  The accumulators start from
+// the bias, so every MMA accumulates.
+//   HL = false: each product of the split (A_hi B_hi, A_hi B_lo, A_lo B_hi) is one MMA
+//               into the same columns; bl = bh + lo_u holds the B_lo rows.
+//   HL = true:  two MMAs, A_hi x [B_hi | B_lo] and A_lo x [B_hi | 0], the B rows
+//               interleaved per kd so that the hi and lo products land in the hh and
+//               hl halves of each slot; bh + lo_u holds the [B_hi | 0] rows.
 //   dcol      first accumulator column of tile 0
 //   ah0, al0  A descriptors (hi, lo) of this A stage, tap offset included
-//   bh0       B descriptor of the stage's first K-step, hi rows of the window
-//   lo_u      distance from hi rows to lo rows (16-byte units)
-template <int T, int KSS>
+//   bh0       B descriptor of the stage's first K-step, first row of the window
+template <int T, int KSS, bool HL>
 static __device__ __forceinline__ void issue_stage(uint32_t dcol, uint32_t tile_cols, uint64_t ah0, uint64_t al0,
                                                    uint64_t bh0, uint32_t lo_u, uint32_t ks_u, uint32_t blk_u,
                                                    uint32_t idesc) {
@@ -137,9 +142,14 @@ static __device__ __forceinline__ void issue_stage(uint32_t dcol, uint32_t tile_
     for (int t = 0; t < T; ++t) {
       const uint32_t dt = dcol + (uint32_t)t * tile_cols;
       const uint64_t ah = ah0 + koff + (uint64_t)(t * 128), al = al0 + koff + (uint64_t)(t * 128);
-      umma_tf32(dt, ah, bh, idesc, 1u);
-      umma_tf32(dt, ah, bl, idesc, 1u);
-      umma_tf32(dt, al, bh, idesc, 1u);
+      if constexpr (HL) {
+        umma_tf32(dt, ah, bh, idesc, 1u);
+        umma_tf32(dt, al, bl, idesc, 1u);
+      } else {
+        umma_tf32(dt, ah, bh, idesc, 1u);
+        umma_tf32(dt, ah, bl, idesc, 1u);
+        umma_tf32(dt, al, bh, idesc, 1u);
+      }
     }
   }
 }
@@ -148,7 +158,7 @@ static __device__ __forceinline__ void issue_stage(uint32_t dcol, uint32_t tile_
 // Streaming weights: one ring stage per tap, waited for, used and released.
 // Resident weights: block (tap_base + khw) * KS + blk0.  Returns false if a wait gave
 // up (the MMAs are still issued, on whatever the buffers hold; the caller stops).
-template <int T, int KSS, bool RES>
+template <int T, int KSS, bool RES, bool HL>
 static __device__ __forceinline__ bool issue_taps(const TcParams& p, uint32_t dcol, uint32_t tile_cols,
                                                   uint64_t ah0, uint64_t al0, uint64_t bwin, uint32_t lo_u,
                                                   uint32_t ks_u, uint32_t blk_u, uint32_t row_u, uint32_t idesc,
@@ -169,7 +179,7 @@ static __device__ __forceinline__ bool issue_taps(const TcParams& p, uint32_t dc
         tc_fence_after();
         bst = bwin + (uint64_t)(rb.idx * b_stage_u);
       }
-      issue_stage<T, KSS>(dcol, tile_cols, ah0 + tap_u, al0 + tap_u, bst, lo_u, ks_u, blk_u, idesc);
+      issue_stage<T, KSS, HL>(dcol, tile_cols, ah0 + tap_u, al0 + tap_u, bst, lo_u, ks_u, blk_u, idesc);
       if constexpr (!RES) {
         umma_commit(&b_empty[rb.idx]);
         rb.next((uint32_t)p.SB);
@@ -199,7 +209,7 @@ static __device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, floa
   asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
-template <int EPI, int KDM, int T, int KSS, bool RES>
+template <int EPI, int KDM, int T, int KSS, bool RES, bool HL>
 __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ uint32_t s_tmem;
@@ -223,7 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   volatile int* abort_flag = &s_abort;
-  const uint32_t tile_cols = (uint32_t)(p.NSLOT * p.Cout);
+  const uint32_t slot_w = (uint32_t)((HL ? 2 : 1) * p.Cout);  // accumulator columns per slot
+  const uint32_t tile_cols = (uint32_t)p.NSLOT * slot_w;
 
   if (tid < p.Cout) s_bias[tid] = p.bias ? p.bias[tid] : 0.0f;
   if (tid == 0) {
@@ -258,8 +269,14 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
     const int grp = (warp - kEpiWarp0) >> 2;
     const uint32_t lane_base = tmem_base + ((uint32_t)((warp & 3) * 32) << 16);
     for (uint32_t c = (uint32_t)grp * 16u; c < (uint32_t)T * tile_cols; c += 32u) {
+      const uint32_t r = c % slot_w;  // column within its slot (HL: hh half, then hl half)
       float bv[16];
-      load_bias16(s_bias + c % (uint32_t)p.Cout, bv);
+      if (r < (uint32_t)p.Cout) {
+        load_bias16(s_bias + r, bv);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) bv[j] = 0.0f;
+      }
       tmem_st16(lane_base + c, bv);
     }
     tmem_wait_st();
@@ -272,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
     // ------------------------------------------------------------ weight producer
     if (lane == 0) {
       if constexpr (RES) {
-        const uint32_t total = (uint32_t)(27 * p.KS) * (p.b_block_bytes / (KDM == 3 ? 3u : 1u));
+        const uint32_t total = p.blob_bytes;
         mbar_arrive_expect_tx(w_full, total);
         const uint8_t* src = reinterpret_cast<const uint8_t*>(p.wblob);
         for (uint32_t off = 0; off < total;) {
@@ -333,13 +350,13 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
       // Descriptors are formed once and advanced by plain adds in 16-byte units (the
       // start-address field is the low 14 bits), so the issue loop stays a short
       // chain of adds and tcgen05.mma.
-      const uint32_t b_rows = (uint32_t)((KDM == 3 ? 6 : 2) * p.Cout);
+      const uint32_t b_rows = (uint32_t)((KDM == 3 ? (HL ? 12 : 6) : 2) * p.Cout);
       const uint64_t a_desc0 = umma_desc_noswizzle(smem_addr(smem_a), (uint32_t)p.NPOS * 16u, 128);
       const uint64_t b_desc0 = umma_desc_noswizzle(smem_addr(smem_b), b_rows * 16u, 128);
       const uint32_t a_stage_u = p.a_stage_bytes >> 4, a_half_u = p.a_half_bytes >> 4;
       const uint32_t ks_u = 2u * (uint32_t)p.NPOS;  // next K-step: two channel groups on
       const uint32_t blk_u = p.b_block_bytes >> 4;
-      const uint32_t lo_u = b_rows >> 1;             // lo rows follow the hi rows
+      const uint32_t lo_u = b_rows >> 1;             // the second half of the rows (lo, or [hi | 0])
       const uint32_t row_u = (uint32_t)p.W;          // one input row (kh step)
       const uint32_t cout = (uint32_t)p.Cout;
       const uint32_t idesc1 = umma_idesc_tf32(128, p.Cout);
@@ -370,15 +387,15 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
               // One window: the accumulators of od = d - kd_hi .. d - kd_lo are adjacent
               // (slots ascend with od), the B rows of kd = kd_hi .. kd_lo too.
               const uint32_t nkd = (uint32_t)(kd_hi - kd_lo + 1);
-              const uint32_t dcol = tmem_base + (s0 + (uint32_t)(d - kd_hi - un.od0)) * cout;
-              const uint32_t idesc = umma_idesc_tf32(128, (int)(nkd * cout));
-              const uint64_t bwin = b_desc0 + (uint64_t)((uint32_t)(2 - kd_hi) * cout);
-              ok = issue_taps<T, KSS, RES>(p, dcol, tile_cols, ah0, al0, bwin, lo_u, ks_u, blk_u, row_u, idesc, 0,
+              const uint32_t dcol = tmem_base + (s0 + (uint32_t)(d - kd_hi - un.od0)) * slot_w;
+              const uint32_t idesc = umma_idesc_tf32(128, (int)(nkd * slot_w));
+              const uint64_t bwin = b_desc0 + (uint64_t)((uint32_t)(2 - kd_hi) * slot_w);
+              ok = issue_taps<T, KSS, RES, HL>(p, dcol, tile_cols, ah0, al0, bwin, lo_u, ks_u, blk_u, row_u, idesc, 0,
                                            ch * KSS, b_full, b_empty, rb, abort_flag);
             } else {
               for (int kd = kd_hi; ok && kd >= kd_lo; --kd) {
                 const uint32_t dcol = tmem_base + slot_add(p, s0, d - kd - un.od0) * cout;
-                ok = issue_taps<T, KSS, RES>(p, dcol, tile_cols, ah0, al0, b_desc0, lo_u, ks_u, blk_u, row_u,
+                ok = issue_taps<T, KSS, RES, false>(p, dcol, tile_cols, ah0, al0, b_desc0, lo_u, ks_u, blk_u, row_u,
                                              idesc1, kd * 9, ch * KSS, b_full, b_empty, rb, abort_flag);
                 if (ok && kd == 2 && ch == p.nchunks - 1) umma_commit(&acc_full[slot_add(p, s0, d - 2 - un.od0)]);
               }
@@ -529,11 +546,23 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
           const int pos = p0 + lp;
           const int oh = pos / p.W, ow = pos - oh * p.W;
           const bool valid = (oh < p.OH) && (ow < p.OW);
-          const uint32_t taddr = lane_base + (uint32_t)t * tile_cols + slot * (uint32_t)p.Cout + (uint32_t)c0;
+          const uint32_t taddr = lane_base + (uint32_t)t * tile_cols + slot * slot_w + (uint32_t)c0;
           float v[16], bv[16];
           tmem_ld16(taddr, v);
+          if constexpr (HL) {
+            float v2[16];
+            tmem_ld16(taddr + (uint32_t)p.Cout, v2);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              v[j] += v2[j];
+              v2[j] = 0.0f;
+            }
+            tmem_st16(taddr + (uint32_t)p.Cout, v2);
+          } else {
+            tmem_wait_ld();
+          }
           load_bias16(s_bias + c0, bv);
-          tmem_wait_ld();
           tmem_st16(taddr, bv);  // the slot's next use starts from the bias again
           if constexpr (EPI != IG3_EPI_POOL_REDUCE) {
             float* yb = p.y + (((size_t)un.n * p.Cout + c0) * p.OD + od) * OHW + (size_t)oh * p.OW + ow;
@@ -613,17 +642,20 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
   }
 }
 
-// Kernel variants: (KDM, T, KSS, resident).  The planner only produces these.
+// Kernel variants: (KDM, HL, T, KSS, resident).  The planner only produces these.
 struct Variant {
-  int kdm, t, kss, res;
+  int kdm, hl, t, kss, res;
 };
 constexpr Variant kVariants[] = {
-    {3, 1, 2, 0}, {3, 2, 2, 0},                                                // streaming, one window per MMA
-    {3, 1, 1, 1}, {3, 1, 2, 1}, {3, 2, 1, 1}, {3, 2, 2, 1}, {3, 4, 1, 1}, {3, 4, 2, 1},  // resident
-    {1, 1, 2, 0}, {1, 1, 1, 0},                                                // streaming, one kd per MMA
+    // one MMA per split product spans the kd window (Cout 48..80)
+    {3, 0, 1, 2, 0}, {3, 0, 2, 2, 0}, {3, 0, 1, 1, 1}, {3, 0, 1, 2, 1}, {3, 0, 2, 1, 1}, {3, 0, 2, 2, 1},
+    // hi and lo products in separate columns: two MMAs span the window (Cout 16, 32)
+    {3, 1, 1, 2, 0}, {3, 1, 2, 2, 0}, {3, 1, 1, 1, 1}, {3, 1, 1, 2, 1}, {3, 1, 2, 1, 1}, {3, 1, 2, 2, 1},
+    // one MMA per kd (Cout 96..128)
+    {1, 0, 1, 2, 0}, {1, 0, 1, 1, 0},
 };
 
-// Launches the kernel variant matching p (KDM, T, KSS, resident).  Returns an ig3 status.
+// Launches the kernel variant matching p.  Returns an ig3 status.
 template <int EPI>
 int launch_kernel(const TcParams& p, size_t smem, int grid, cudaStream_t stream) {
   auto go = [&](auto kernel) -> int {
@@ -632,21 +664,26 @@ int launch_kernel(const TcParams& p, size_t smem, int grid, cudaStream_t stream)
     kernel<<<grid, kThreads, smem, stream>>>(p);
     return count_launch(cuda_status(cudaGetLastError(), "conv3d TC kernel launch"));
   };
-  const int key = p.KDM * 1000 + p.T * 100 + p.KSS * 10 + p.resident;
+  const int key = p.KDM * 10000 + p.HL * 1000 + p.T * 100 + p.KSS * 10 + p.resident;
   switch (key) {
-    case 3120: return go(conv3d_tc_kernel<EPI, 3, 1, 2, false>);
-    case 3220: return go(conv3d_tc_kernel<EPI, 3, 2, 2, false>);
-    case 3111: return go(conv3d_tc_kernel<EPI, 3, 1, 1, true>);
-    case 3121: return go(conv3d_tc_kernel<EPI, 3, 1, 2, true>);
-    case 3211: return go(conv3d_tc_kernel<EPI, 3, 2, 1, true>);
-    case 3221: return go(conv3d_tc_kernel<EPI, 3, 2, 2, true>);
-    case 3411: return go(conv3d_tc_kernel<EPI, 3, 4, 1, true>);
-    case 3421: return go(conv3d_tc_kernel<EPI, 3, 4, 2, true>);
-    case 1120: return go(conv3d_tc_kernel<EPI, 1, 1, 2, false>);
-    case 1110: return go(conv3d_tc_kernel<EPI, 1, 1, 1, false>);
+    case 30120: return go(conv3d_tc_kernel<EPI, 3, 1, 2, false, false>);
+    case 30220: return go(conv3d_tc_kernel<EPI, 3, 2, 2, false, false>);
+    case 30111: return go(conv3d_tc_kernel<EPI, 3, 1, 1, true, false>);
+    case 30121: return go(conv3d_tc_kernel<EPI, 3, 1, 2, true, false>);
+    case 30211: return go(conv3d_tc_kernel<EPI, 3, 2, 1, true, false>);
+    case 30221: return go(conv3d_tc_kernel<EPI, 3, 2, 2, true, false>);
+    case 31120: return go(conv3d_tc_kernel<EPI, 3, 1, 2, false, true>);
+    case 31220: return go(conv3d_tc_kernel<EPI, 3, 2, 2, false, true>);
+    case 31111: return go(conv3d_tc_kernel<EPI, 3, 1, 1, true, true>);
+    case 31121: return go(conv3d_tc_kernel<EPI, 3, 1, 2, true, true>);
+    case 31211: return go(conv3d_tc_kernel<EPI, 3, 2, 1, true, true>);
+    case 31221: return go(conv3d_tc_kernel<EPI, 3, 2, 2, true, true>);
+    case 10120: return go(conv3d_tc_kernel<EPI, 1, 1, 2, false, false>);
+    case 10110: return go(conv3d_tc_kernel<EPI, 1, 1, 1, false, false>);
     default:
-      return fail(IG3_ERR_UNSUPPORTED, "conv3d TC: no kernel variant for KDM %d, T %d, %d K-steps, resident %d",
-                  p.KDM, p.T, p.KSS, p.resident);
+      return fail(IG3_ERR_UNSUPPORTED,
+                  "conv3d TC: no kernel variant for KDM %d, HL %d, T %d, %d K-steps, resident %d", p.KDM, p.HL, p.T,
+                  p.KSS, p.resident);
   }
 }
 
