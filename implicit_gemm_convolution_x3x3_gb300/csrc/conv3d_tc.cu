@@ -139,26 +139,28 @@ struct Plan {
 
 int positions_tiles(int OH, int W, int T) { return ((OH * W) + T * 128 - 1) / (T * 128); }
 
-// Cycle estimate of one input plane's MMAs (per SM): nkd output planes fed, per
-// (tap, K-step, tile) three MMAs (two with HL).  A tcgen05.mma takes ~46 cycles to
-// issue from one thread (small-N MMAs measure nearer 70) and N/2 cycles to execute
-// (M = 128, K = 8); every streamed weight stage adds ~250 cycles of wait and commit to
-// the issuing thread.
-double plane_cycles(int kdm, int hl, int nkd, int Cout, int KS, int nchunks, int T, bool res) {
-  const double issue_one = 46.0;
+// Cycle estimate of one input plane (per SM): nkd output planes fed; per (tap, K-step,
+// tile) three MMAs (two with HL).  Measured inside the kernel, an MMA costs about
+// max(70, N/2 + 5) cycles (one thread issues them; N/2 is the M = 128, K = 8 execution
+// time) and every streamed weight stage ~250 more.  The chunk's input convert runs
+// alongside: ~0.9 cycles per value when the convert warps load x themselves (latency
+// bound), ~0.35 when a bulk-copy loader stages it ahead.
+double plane_cycles(int kdm, int hl, int nkd, int Cout, int KS, int nchunks, int T, bool res, int npos, bool xstage) {
   const int mmas_per_step = (kdm == 3) ? (hl ? 2 : 3) : 3 * nkd;
   const int n = (kdm == 3) ? nkd * Cout * (hl ? 2 : 1) : Cout;
-  const double exec = 9.0 * KS * T * mmas_per_step * std::max(issue_one, 0.5 * n);
+  const double mmas = 9.0 * KS * T * mmas_per_step;
   const double stages = res ? 0.0 : 9.0 * nchunks * (kdm == 3 ? 1 : nkd);
-  const double issue = 9.0 * KS * T * mmas_per_step * issue_one + 250.0 * stages;
-  return std::max(exec, issue) + 300.0 * nchunks;  // A hand-over per chunk
+  const double mma = mmas * std::max(70.0, 0.5 * n + 5.0) + 250.0 * stages;
+  const double conv = (xstage ? 0.35 : 0.9) * npos * (8.0 * KS);
+  return std::max(mma, conv) + 300.0 * nchunks;  // A hand-over per chunk
 }
 
-double unit_cycles(int kdm, int hl, int planes, int Cout, int KS, int nchunks, int T, bool res) {
+double unit_cycles(int kdm, int hl, int planes, int Cout, int KS, int nchunks, int T, bool res, int npos,
+                   bool xstage) {
   double c = 0.0;
   for (int d = 0; d < planes + 2; ++d) {
     const int kd_hi = std::min(2, d), kd_lo = std::max(0, d - planes + 1);
-    c += plane_cycles(kdm, hl, kd_hi - kd_lo + 1, Cout, KS, nchunks, T, res);
+    c += plane_cycles(kdm, hl, kd_hi - kd_lo + 1, Cout, KS, nchunks, T, res, npos, xstage);
   }
   return c;
 }
@@ -199,8 +201,8 @@ Plan make_plan_uncached(int N, int Cin, int D, int H, int W, int Cout, int epi, 
     const uint32_t epi_bytes = (epi == IG3_EPI_POOL_REDUCE) ? (uint32_t)(2 * 16 * 32 + T * Cout * 32) * 4u : 0u;
     const uint32_t off_b = kAStages * a_stage;
     // 2 KB for static shared memory and alignment; barriers for the largest ring.
-    const long long avail =
-        (long long)kSmemLimit - off_b - epi_bytes - 2048 - 128 - (6 + 2 * nslot + 2 * kMaxStages) * 8;
+    const long long avail = (long long)kSmemLimit - off_b - epi_bytes - 2048 - 128 - 128 -
+                            (6 + 2 * nslot + 2 * kMaxStages + 2 * kMaxXStages) * 8;
     if (avail <= 0) continue;
     int sb = 0;
     if (res) {
@@ -209,6 +211,11 @@ Plan make_plan_uncached(int N, int Cin, int D, int H, int W, int Cout, int epi, 
       sb = (int)std::min<long long>(kMaxStages, avail / ((long long)kss * blk));
       if (sb < 3) continue;
     }
+    // Raw input stages for the bulk-copy loader in what is left (at least two).
+    const uint32_t x_stage = (uint32_t)(8 * kss) * npos * 4u;
+    const long long left = avail - (res ? (long long)blob : (long long)sb * kss * blk);
+    int xs = (int)std::min<long long>(kMaxXStages, left / x_stage);
+    if (xs < 2) xs = 0;
     // Planes per unit: with KDM 3 a unit's planes must fit the slots.
     const int pmax = (kdm == 3) ? std::min(OD, nslot) : OD;
     const int G = positions_tiles(OH, W, T);
@@ -217,8 +224,8 @@ Plan make_plan_uncached(int N, int Cin, int D, int H, int W, int Cout, int epi, 
       const int last = OD - (S - 1) * P;
       const long long units = (long long)N * G * S;
       const int grid = (int)std::min<long long>(units, sms);
-      const double c_full = unit_cycles(kdm, hl, P, Cout, KS, nchunks, T, res);
-      const double c_last = unit_cycles(kdm, hl, last, Cout, KS, nchunks, T, res);
+      const double c_full = unit_cycles(kdm, hl, P, Cout, KS, nchunks, T, res, npos, xs > 0);
+      const double c_last = unit_cycles(kdm, hl, last, Cout, KS, nchunks, T, res, npos, xs > 0);
       // Round-robin over the grid: CTA c takes units c, c + grid, ...; a unit is
       // the last split iff u % S == S - 1.
       double worst = 0.0;
@@ -253,9 +260,12 @@ Plan make_plan_uncached(int N, int Cin, int D, int H, int W, int Cout, int epi, 
         p.b_block_bytes = blk;
         p.blob_bytes = blob;
         p.off_b = off_b;
+        p.XS = xs;
+        p.x_stage_bytes = x_stage;
         p.off_epi = off_b + (res ? blob : (uint32_t)sb * kss * blk);
-        p.off_bar = (p.off_epi + epi_bytes + 127) / 128 * 128;
-        pl.smem = std::max<size_t>(p.off_bar + (6 + 2 * (size_t)nslot + 2 * (size_t)sb) * 8, kMinSmem);
+        p.off_x = (p.off_epi + epi_bytes + 127) / 128 * 128;
+        p.off_bar = p.off_x + (uint32_t)xs * x_stage;
+        pl.smem = std::max<size_t>(p.off_bar + (6 + 2 * (size_t)nslot + 2 * (size_t)sb + 2 * (size_t)xs) * 8, kMinSmem);
         pl.ok = true;
       }
     }
@@ -320,6 +330,7 @@ int conv3d_tc_launch(const Conv3dArgs& a) {
   p.partial = reinterpret_cast<float*>(ws + pl.blob_bytes);
   p.inv_div = (a.epi == IG3_EPI_POOL_REDUCE) ? 1.0f / a.divisor : 1.0f;
   p.vec = ((size_t)a.H * a.W % 4 == 0 && reinterpret_cast<uintptr_t>(a.x) % 16 == 0) ? 1 : 0;
+  if (!p.vec) p.XS = 0;  // bulk copies need 16-byte aligned rows
   p.ctl = wait_ctl();
   if (!p.ctl.status) return fail(IG3_ERR_CUDA, "conv3d TC path: device status word unavailable");
 

@@ -17,6 +17,7 @@ constexpr int kAStages = 2;
 constexpr int kTmemCols = 512;
 constexpr int kMaxSlots = 32;  // accumulator slots per position tile (one parity bit each)
 constexpr int kMaxStages = 8;  // weight ring stages
+constexpr int kMaxXStages = 4; // raw input stages
 constexpr int kSmemLimit = 227 * 1024;
 constexpr int kMinSmem = 116 * 1024;  // keeps one CTA (one TMEM owner) per SM
 
@@ -39,6 +40,7 @@ struct TcParams {
   int units;
   int resident;  // weights loaded once
   int SB;        // weight ring stages (streaming)
+  int XS;        // raw input stages of the bulk-copy loader (0: convert warps load x)
   int epi;
   int vec;       // x planes 16-byte aligned with H*W % 4 == 0: convert with 16-byte loads
   float inv_div;
@@ -46,7 +48,8 @@ struct TcParams {
   uint32_t a_stage_bytes;  // hi + lo
   uint32_t b_block_bytes;  // one K-step block of B
   uint32_t blob_bytes;     // all blocks (resident weights)
-  uint32_t off_b, off_epi, off_bar;  // shared-memory offsets
+  uint32_t x_stage_bytes;  // one raw input stage: [CC channels][NPOS positions] floats
+  uint32_t off_b, off_epi, off_x, off_bar;  // shared-memory offsets
   WaitCtl ctl;
 };
 
@@ -229,6 +232,11 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
   uint64_t* acc_empty = acc_full + p.NSLOT;    // [NSLOT]
   uint64_t* b_full = acc_empty + p.NSLOT;      // [SB]
   uint64_t* b_empty = b_full + p.SB;           // [SB]
+  uint64_t* x_full = b_empty + p.SB;           // [XS]
+  uint64_t* x_empty = x_full + p.XS;           // [XS]
+  // With the bulk-copy loader, the first convert warp issues the copies and the other
+  // five transform; otherwise all six load and transform.
+  const int conv_threads = kConvThreads - (p.XS > 0 ? 32 : 0);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -240,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
   if (tid == 0) {
     s_abort = 0;
     for (int i = 0; i < kAStages; ++i) {
-      mbar_init(&a_full[i], kConvThreads);
+      mbar_init(&a_full[i], conv_threads);
       mbar_init(&a_empty[i], 1);
     }
     mbar_init(w_full, 1);
@@ -252,6 +260,10 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
     for (int i = 0; i < p.SB; ++i) {
       mbar_init(&b_full[i], 1);
       mbar_init(&b_empty[i], 1);
+    }
+    for (int i = 0; i < p.XS; ++i) {
+      mbar_init(&x_full[i], 1);
+      mbar_init(&x_empty[i], conv_threads);
     }
     fence_mbarrier_init();
   }
@@ -415,11 +427,58 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
     }
   } else if (warp < kEpiWarp0) {
     // ------------------------------------------------------------ input convert
-    const int ct = tid - kConvWarp0 * 32;
     const size_t HW = (size_t)p.H * p.W;
     const int plane_pos = p.H * p.W;
     const int CC = KSS * 8;
-    Ring ra;
+    if (p.XS > 0 && warp == kConvWarp0) {
+      // Input loader (one thread): for each (plane, chunk) the CC channel rows of the
+      // NPOS positions the unit needs, each a contiguous run of x, by 1-D bulk copy
+      // into a ring of raw stages [CC][NPOS], up to XS chunks ahead of the transform.
+      // Rows end at the plane's last position; channels past Cin are not copied.
+      if (lane == 0) {
+        Ring rx;
+        uint32_t issued = 0;
+        uint8_t* smem_x = smem + p.off_x;
+        for (int u = blockIdx.x; u < p.units && !*abort_flag; u += gridDim.x) {
+          const Unit un = decode_unit(p, u);
+          const int p0 = un.g * T * 128;
+          const uint32_t row_bytes = (uint32_t)min(p.NPOS, plane_pos - p0) * 4u;
+          for (int d = un.od0; d < un.od1 + 2; ++d) {
+            for (int ch = 0; ch < p.nchunks; ++ch) {
+              if (!wait_fast(&x_empty[rx.idx], rx.phase ^ 1u, p.ctl, abort_flag)) goto loader_done;
+              const int c0 = ch * CC;
+              const int nvalid = min(CC, p.Cin - c0);
+              mbar_arrive_expect_tx(&x_full[rx.idx], (uint32_t)nvalid * row_bytes);
+              const float* src = p.x + (((size_t)un.n * p.Cin + c0) * p.D + d) * HW + p0;
+              uint8_t* dst = smem_x + (size_t)rx.idx * p.x_stage_bytes;
+              for (int c = 0; c < nvalid; ++c)
+                bulk_copy_g2s(dst + (size_t)c * p.NPOS * 4, src + (size_t)c * p.D * HW, row_bytes, &x_full[rx.idx]);
+              rx.next((uint32_t)p.XS);
+              ++issued;
+            }
+          }
+        }
+      loader_done:
+        if (*abort_flag) {
+          // Let every copy still in flight land before the CTA can exit.
+          Ring back = rx;
+          const uint32_t outstanding = min(issued, (uint32_t)p.XS);
+          for (uint32_t i = 0; i < outstanding; ++i) {
+            if (back.idx == 0) {
+              back.idx = p.XS - 1;
+              back.phase ^= 1u;
+            } else {
+              --back.idx;
+            }
+            drain_wait(&x_full[back.idx], back.phase, p.ctl);
+          }
+        }
+      }
+      goto convert_done;
+    }
+    {
+    const int ct = tid - (kConvWarp0 + (p.XS > 0 ? 1 : 0)) * 32;
+    Ring ra, rx;
     for (int u = blockIdx.x; u < p.units && !*abort_flag; u += gridDim.x) {
       const Unit un = decode_unit(p, u);
       const int p0 = un.g * T * 128;
@@ -431,7 +490,43 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
           const uint32_t hi_base = smem_addr(smem_a) + ra.idx * p.a_stage_bytes;
           const uint32_t lo_base = hi_base + p.a_half_bytes;
           const float* xplane = p.x + ((size_t)un.n * p.Cin) * p.D * HW + (size_t)d * HW;
-          if (p.vec) {
+          if (p.XS > 0) {
+            // Transform a raw stage: item = (channel group, 4 consecutive positions),
+            // four 16-byte shared loads (one per channel), split, transposed to four
+            // [position][4 channels] entries.  Positions past the plane and channels
+            // past Cin read as zero.
+            if (!warp_wait(&x_full[rx.idx], rx.phase, p.ctl, abort_flag)) goto convert_done;
+            const float* raw = reinterpret_cast<const float*>(smem + p.off_x + (size_t)rx.idx * p.x_stage_bytes);
+            const int quads = p.NPOS >> 2;
+            const int vitems = (CC / 4) * quads;
+            for (int i = ct; i < vitems; i += conv_threads) {
+              const int grp = i / quads, qd = i - grp * quads;
+              const bool in_plane = p0 + 4 * qd < plane_pos;
+              float4 v[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int cl = grp * 4 + j;
+                v[j] = (in_plane && c0 + cl < p.Cin) ? *reinterpret_cast<const float4*>(raw + cl * p.NPOS + 4 * qd)
+                                                     : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+              }
+              const uint32_t off = (uint32_t)(grp * p.NPOS + 4 * qd) * 16u;
+              float h[4][4], l[4][4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                split_tf32(v[j].x, h[0][j], l[0][j]);
+                split_tf32(v[j].y, h[1][j], l[1][j]);
+                split_tf32(v[j].z, h[2][j], l[2][j]);
+                split_tf32(v[j].w, h[3][j], l[3][j]);
+              }
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                st_shared_v4(hi_base + off + 16u * e, h[e][0], h[e][1], h[e][2], h[e][3]);
+                st_shared_v4(lo_base + off + 16u * e, l[e][0], l[e][1], l[e][2], l[e][3]);
+              }
+            }
+            mbar_arrive(&x_empty[rx.idx]);
+            rx.next((uint32_t)p.XS);
+          } else if (p.vec) {
             // Item = (channel group, 4 consecutive positions): four 16-byte loads (one
             // per channel, coalesced along positions), transposed in registers to four
             // [position][4 channels] entries.  H*W % 4 == 0, so a quad lies wholly inside
@@ -509,6 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
           ra.next(kAStages);
         }
       }
+    }
     }
   convert_done:;
   } else {
