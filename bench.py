@@ -131,14 +131,21 @@ def traffic_for(kernel_key: str, wl_name: str):
             rec = json.load(f).get(kernel_key, {}).get(wl_name)
     except (OSError, ValueError):
         return None
-    if not rec:
+    if not rec or not rec.get("sources") or not rec.get("sources_sha256"):
         return None
-    src = os.path.join(ROOT, rec["source"])
+    return rec["dram_bytes_per_launch"] if sources_sha256(rec["sources"]) == rec["sources_sha256"] else None
+
+
+def sources_sha256(paths):
+    """sha256 over the named source files, in order (None if one is missing)."""
+    h = hashlib.sha256()
     try:
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        for rel in paths:
+            with open(os.path.join(ROOT, rel), "rb") as f:
+                h.update(f.read())
     except OSError:
         return None
-    return rec["dram_bytes_per_launch"] if h == rec.get("source_sha256") else None
+    return h.hexdigest() if paths else None
 
 
 # ------------------------------------------------------------------ clocks

@@ -58,6 +58,11 @@ SMALL_CASES = [
     (2, 16, 4, 9, 8, 16),     # narrow rows (W = 8)
     (1, 16, 4, 6, 64, 128),   # Cout = 128
     (1, 24, 3, 7, 33, 48),    # Cin not a multiple of 8, Cout = 48
+    (1, 40, 5, 10, 32, 32),   # Cout = 32: hi and lo products in separate accumulator columns
+    (1, 5, 4, 11, 13, 80),    # Cout = 80: the widest three-plane window (N = 240)
+    (1, 12, 5, 8, 20, 96),    # Cout = 96: one MMA per kd over a ring of five slots
+    (1, 8, 6, 9, 16, 112),    # Cout = 112: one MMA per kd, four slots
+    (2, 72, 4, 6, 24, 64),    # Cin = 72: several channel chunks of streamed weights
     (2, 3, 5, 7, 9, 5),       # odd channel counts
     (1, 1, 3, 3, 3, 1),       # smallest valid input: one output
 ]
@@ -195,3 +200,33 @@ def test_errors_are_reported_not_raised_on_device(ig3):
     assert e.value.status == -2  # Cout = 2 is not a tensor-core shape
     torch.cuda.synchronize()
     assert ig3.ig3_last_device_status() == 0
+
+
+@pytest.mark.parametrize("shape,epi", [((1, 8, 6, 10, 64, 16), "pool_reduce"), ((1, 32, 5, 8, 64, 64), "tanh_mish"),
+                                       ((1, 16, 5, 9, 16, 32), "tanh_mish")],
+                         ids=["pool-resident", "streamed", "split-columns"])
+def test_conv3d_misaligned_input(ig3, shape, epi):
+    """x 4 bytes off a 16-byte boundary: the convert falls back from 16-byte loads and
+    from the bulk-copy loader to scalar loads; results must not change."""
+    N, Cin, D, H, W, Cout = shape
+    wl = si.conv3d_workload("t", N, Cin, D, H, W, Cout, seed=5000 + sum(shape), epilogue=epi,
+                            bias2=(epi == "pool_reduce"))
+    t = wl.generate_all()
+    params = {"divisor": 2.0, "pool": 2} if epi == "pool_reduce" else None
+    if epi == "pool_reduce":
+        ref = oracle.conv3d_pool_reduce(t["x"], t["w"], t["b"], 2.0, 2, t["bias2"])
+    else:
+        ref = oracle.tanh_mish(oracle.conv3d(t["x"], t["w"], t["b"]))
+    buf = torch.empty(t["x"].size + 1, dtype=torch.float32, device="cuda")
+    x = buf[1:].view(t["x"].shape)
+    x.copy_(torch.from_numpy(t["x"]))
+    assert x.data_ptr() % 16 != 0
+    w = to_dev(t["w"]); b = to_dev(t["b"])
+    dev_params = None
+    if params is not None:
+        dev_params = dict(params)
+        dev_params["bias2"] = to_dev(t["bias2"])
+    for path in paths_for(ig3, shape, epi):
+        out = ig3.conv3d_fused(x, w, b, epilogue=epi, params=dev_params, path=path)
+        assert ig3.ig3_last_device_status() == 0
+        assert_close(out.cpu().numpy(), ref, f"misaligned {shape} {epi} {path}")
