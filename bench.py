@@ -265,12 +265,24 @@ def time_steps(call, steps: int, warmup: int, dist_on: bool):
     t1 = time.time()
     if dist_on:
         dist.barrier()
-    ms = start.elapsed_time(end)
-    if dist_on:
-        v = torch.tensor([ms], device="cuda", dtype=torch.float64)
-        dist.all_reduce(v, op=dist.ReduceOp.MAX)
-        ms = float(v.item())
+    ms = max_over_ranks(start.elapsed_time(end), dist_on)
     return ms, t0, t1
+
+
+def max_over_ranks(value: float, dist_on: bool, device: str = "cuda") -> float:
+    """The largest `value` over all ranks: the job takes as long as its slowest rank."""
+    if not dist_on:
+        return value
+    import torch
+    import torch.distributed as dist
+    v = torch.tensor([value], device=device, dtype=torch.float64)
+    dist.all_reduce(v, op=dist.ReduceOp.MAX)
+    return float(v.item())
+
+
+def job_gflops(flop_per_rank: float, world: int, us_per_step: float) -> float:
+    """Whole-job throughput: the work of every rank over the (slowest rank's) step time."""
+    return flop_per_rank * world / (us_per_step * 1e-6) / 1e9
 
 
 def e2e_steps(ig3, wl, call, dev_t: dict, out, steps: int, warmup: int):
@@ -311,7 +323,7 @@ def measure_workload(ig3, wl, path, steps, warmup, peaks, src, rank=0, world=1, 
     per_step_launches = launches // (steps + warmup) if steps + warmup else 0
     flop = 2.0 * macs(wl)
     us = ms * 1e3 / steps
-    gflops = flop * world / (us * 1e-6) / 1e9
+    gflops = job_gflops(flop, world, us)
     roof = roofline_peak(chosen, wl.op, peaks, src)
     if roof["unit"] == "GB/s":
         rd, wr = compulsory_bytes(wl)
