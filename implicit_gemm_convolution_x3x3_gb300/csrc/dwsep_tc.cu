@@ -1,5 +1,5 @@
 // Depthwise 3x3 (stride 1, pad 1) -> pointwise 1x1 on sm_103a, fused in one kernel:
-// the depthwise result goes from registers to shared memory and straight into a
+// the depthwise result goes from registers into tensor memory and straight into a
 // tcgen05 GEMM; it never reaches HBM ("Kimi-K2.6__l1_p86": the per-output
 // pseudo-code, and the note that fusing removes the intermediate's write and read).
 //
@@ -7,48 +7,62 @@
 //   y[n,o,h,w]  = sum_c w_pw[o,c] * dw[n,c,h,w] (+ b[o])
 //
 // Tile = 128 consecutive pixels of one image row (GEMM M = 128, N = Cout, K = C).
-// Persistent CTAs (one per SM, 416 threads) walk strips of rows, so the rows above
-// and below a tile were read for the previous tile and come from L2, not HBM.
+// A work unit is a strip of R rows of one 128-pixel column segment; persistent CTAs
+// (one per SM, 448 threads) walk units.
 //   warp 0      TMEM owner and MMA issuer (one thread);
-//   warps 1-8   depthwise: lane l owns pixels l, l+32, l+64, l+96 of 4 channels;
-//               each input row is one coalesced load per 32 pixels, the left and
-//               right neighbours come by warp shuffle; the 3x3 sums are split into
-//               tf32 hi/lo and stored K-major [channel group][pixel][4], with
-//               consecutive lanes writing consecutive 16-byte rows (no bank conflicts);
-//   warps 9-12  epilogue: tcgen05.ld from a double-buffered TMEM accumulator,
-//               + bias, one full 128-byte line per warp store.
-// The pointwise weights are split into [hi ; lo] rows once per CTA and stay in
-// shared memory; acc = A_hi*[B_hi|B_lo] + A_lo*B_hi (3xTF32, as in conv3d_tc.cu).
-// With tensor cores doing the pointwise sums the kernel is bound by HBM traffic
-// (read x once, write y once).  Every wait is bounded.
+//   warp 1      row loader (one thread): each input row the strip needs (rows h0-1 ..
+//               h0+R) as one tensor-map bulk copy of [C channels][136 pixels]
+//               (pixels w0-4 .. w0+131) into a ring of four shared-memory row slots;
+//               rows or pixels outside the image come back as zeros, which is the
+//               padding;
+//   warps 2-9   depthwise: lane = pixel (TMEM lane = GEMM row), two warps per TMEM
+//               lane quadrant, each taking half of the channels: nine shared-memory
+//               reads and FMAs per (pixel, channel), the sums split into tf32 hi/lo
+//               and written to tensor memory as the GEMM's A operand;
+//   warps 10-13 epilogue: tcgen05.ld of a double-buffered accumulator, + bias, one
+//               128-byte line per warp store.
+// Tensor memory: accumulators at columns [0, 2*Cout), A tiles (hi | lo, C columns
+// each, double-buffered) at [256, 256 + 4*C).  The pointwise weights are split into
+// [hi ; lo] rows once per CTA and stay in shared memory; the GEMM takes A from tensor
+// memory and B from shared memory: acc = A_hi*B_hi + A_hi*B_lo + A_lo*B_hi (3xTF32, as
+// in conv3d_tc.cu), three MMAs of N = Cout per 8 channels.  The kernel is meant to be
+// bound by HBM traffic (read x once, write y once).  Every wait is bounded.
 #include <algorithm>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include "ig3_internal.h"
 
 namespace ig3 {
 namespace {
 
-constexpr int kThreads = 416;
-constexpr int kDwWarp0 = 1, kDwThreads = 256;
-constexpr int kEpiWarp0 = 9, kEpiThreads = 128;
-constexpr int kRows = 8;        // image rows per work unit
+constexpr int kThreads = 448;
+constexpr int kMmaWarp = 0, kLoadWarp = 1;
+constexpr int kDwWarp0 = 2, kDwWarps = 8;
+constexpr int kEpiWarp0 = 10, kEpiThreads = 128;
 constexpr int kTile = 128;      // pixels per tile
+constexpr int kHalo = 4;        // staged columns on each side (keeps the copy 16-byte aligned)
+constexpr int kBoxW = kTile + 2 * kHalo;
+constexpr int kRowSlots = 4;
 constexpr int kTmemCols = 512;
+constexpr int kACol0 = 256;     // first TMEM column of the A tiles
 
 struct DwParams {
-  const float* x;
   const float* w_dw;
   const float* w_pw;
   const float* bias;
   float* y;
   int N, C, H, W, Cout;
-  int WB;         // tiles per image row
-  int HR;         // row strips per image
+  int WB;         // 128-pixel segments per image row
+  int R;          // rows per strip
+  int HR;         // strips per image column
   int units;
-  int prefetch;   // rows start on 16-byte boundaries, so bulk L2 prefetches are legal
-  uint32_t a_half_bytes, a_stage_bytes, off_b, off_wdw, off_bar;
+  uint32_t row_bytes;                       // one staged row: C x kBoxW floats
+  uint32_t off_wdw, off_rows, off_bar;      // shared-memory offsets (B at 0)
   WaitCtl ctl;
 };
 
@@ -82,24 +96,51 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __all_sync(0xffffffffu, ok) != 0;
 }
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, float b, float c, float d) {
-  asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+// 3-D tiled bulk copy (TMA) global -> shared, completion counted in bytes on `bar`.
+// Coordinates are in elements, innermost first; parts of the box outside the tensor
+// read as zeros.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+      : "memory");
 }
 
-__global__ void __launch_bounds__(kThreads, 1) dwsep_tc_kernel(const DwParams p) {
+// D[tmem] (+)= A[tmem] * B[smem]^T, issued by one thread (A: 128 lanes x 8 columns).
+__device__ __forceinline__ void umma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 32 lanes x 4 consecutive columns from registers (thread i -> lane 32*(warp%4) + i).
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, float a, float b, float c, float d) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    dwsep_tc_kernel(const DwParams p, const __grid_constant__ CUtensorMap xmap) {
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
 
-  uint8_t* smem_a = smem;
-  uint8_t* smem_b = smem + p.off_b;
+  uint8_t* smem_b = smem;
   float* s_wdw = reinterpret_cast<float*>(smem + p.off_wdw);
+  uint8_t* smem_rows = smem + p.off_rows;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
-  uint64_t* a_full = bars;        // [2]
-  uint64_t* a_empty = bars + 2;   // [2]
-  uint64_t* acc_full = bars + 4;  // [2]
-  uint64_t* acc_empty = bars + 6; // [2]
-  uint64_t* mma_done = bars + 8;
+  uint64_t* row_full = bars;                 // [kRowSlots]
+  uint64_t* row_empty = bars + kRowSlots;    // [kRowSlots]
+  uint64_t* a_full = bars + 2 * kRowSlots;   // [2]
+  uint64_t* a_empty = a_full + 2;            // [2]
+  uint64_t* acc_full = a_full + 4;           // [2]
+  uint64_t* acc_empty = a_full + 6;          // [2]
+  uint64_t* mma_done = a_full + 8;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -108,8 +149,12 @@ __global__ void __launch_bounds__(kThreads, 1) dwsep_tc_kernel(const DwParams p)
 
   if (tid == 0) {
     s_abort = 0;
+    for (int i = 0; i < kRowSlots; ++i) {
+      mbar_init(&row_full[i], 1);
+      mbar_init(&row_empty[i], kDwWarps);
+    }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&a_full[i], kDwThreads);
+      mbar_init(&a_full[i], kDwWarps);
       mbar_init(&a_empty[i], 1);
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], kEpiThreads);
@@ -117,14 +162,14 @@ __global__ void __launch_bounds__(kThreads, 1) dwsep_tc_kernel(const DwParams p)
     mbar_init(mma_done, 1);
     fence_mbarrier_init();
   }
-  if (warp == 0) {
+  if (warp == kMmaWarp) {
     tmem_alloc(&s_tmem, kTmemCols);
     tmem_relinquish();
   }
-  // Pointwise weights -> [K-step][k-half][2*Cout rows: hi, lo][4]; depthwise weights.
+  // Pointwise weights -> [K-step][k-half][2*Cout rows: hi, lo][4]; depthwise weights
+  // padded to [C][3 rows][4] so that one 16-byte load yields a row of the 3x3 kernel.
   {
-    const int ks_n = C >> 3;
-    const int total = ks_n * 2 * (2 * Cout) * 4;
+    const int total = (C >> 3) * 2 * (2 * Cout) * 4;
     float* sb = reinterpret_cast<float*>(smem_b);
     for (int i = tid; i < total; i += kThreads) {
       const int j = i & 3;
@@ -139,43 +184,42 @@ __global__ void __launch_bounds__(kThreads, 1) dwsep_tc_kernel(const DwParams p)
       split_tf32(__ldg(&p.w_pw[(size_t)co * C + c]), hi, lo);
       sb[i] = (row < Cout) ? hi : lo;
     }
-    for (int i = tid; i < C * 9; i += kThreads) s_wdw[i] = __ldg(&p.w_dw[i]);
+    for (int i = tid; i < C * 12; i += kThreads) {
+      const int c = i / 12, r = (i % 12) >> 2, k = i & 3;
+      s_wdw[i] = (k < 3) ? __ldg(&p.w_dw[c * 9 + r * 3 + k]) : 0.0f;
+    }
     fence_proxy_async_smem();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = s_tmem;
-  const int HW = p.H * p.W;
 
-  if (warp == 0) {
+  if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc_cat = umma_idesc_tf32(128, 2 * Cout);
-      const uint32_t idesc_one = umma_idesc_tf32(128, Cout);
-      const uint64_t a_desc0 = umma_desc_noswizzle(smem_addr(smem_a), (uint32_t)kTile * 16u, 128);
+      const uint32_t idesc = umma_idesc_tf32(128, Cout);
       const uint64_t b_desc0 = umma_desc_noswizzle(smem_addr(smem_b), (uint32_t)(2 * Cout) * 16u, 128);
-      const uint32_t a_stage_u = p.a_stage_bytes >> 4, a_half_u = p.a_half_bytes >> 4;
-      const uint32_t ks_a_u = 2u * kTile;            // two channel groups of 128 rows
       const uint32_t ks_b_u = (uint32_t)(4 * Cout);  // one B block: 2 halves x 2*Cout rows x 16 B
+      const uint32_t lo_u = (uint32_t)Cout;          // lo rows follow the hi rows
       const int ks_n = C >> 3;
       Ring ra, racc;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
         const int hr = u % p.HR;
-        const int h0 = hr * kRows, h1 = min(p.H, h0 + kRows);
+        const int h0 = hr * p.R, h1 = min(p.H, h0 + p.R);
         for (int h = h0; ok && h < h1; ++h) {
           if (!(ok = wait_fast(&a_full[ra.idx], ra.phase, p.ctl, abort_flag))) break;
           if (!(ok = wait_fast(&acc_empty[racc.idx], racc.phase ^ 1u, p.ctl, abort_flag))) break;
           tc_fence_after();
-          const uint64_t ah = a_desc0 + (uint64_t)(ra.idx * a_stage_u);
-          const uint64_t al = ah + a_half_u;
-          const uint32_t d = tmem_base + racc.idx * (uint32_t)(2 * Cout);
+          const uint32_t a_hi = tmem_base + (uint32_t)kACol0 + ra.idx * (uint32_t)(2 * C);
+          const uint32_t a_lo = a_hi + (uint32_t)C;
+          const uint32_t d = tmem_base + racc.idx * (uint32_t)Cout;
           for (int ks = 0; ks < ks_n; ++ks) {
-            const uint64_t ko = (uint64_t)((uint32_t)ks * ks_a_u);
             const uint64_t bh = b_desc0 + (uint64_t)((uint32_t)ks * ks_b_u);
-            umma_tf32(d, ah + ko, bh, idesc_cat, ks > 0 ? 1u : 0u);
-            umma_tf32(d, al + ko, bh, idesc_one, 1u);
+            umma_tf32_ts(d, a_hi + 8u * ks, bh, idesc, ks > 0 ? 1u : 0u);
+            umma_tf32_ts(d, a_hi + 8u * ks, bh + lo_u, idesc, 1u);
+            umma_tf32_ts(d, a_lo + 8u * ks, bh, idesc, 1u);
           }
           umma_commit(&a_empty[ra.idx]);
           umma_commit(&acc_full[racc.idx]);
@@ -187,104 +231,111 @@ __global__ void __launch_bounds__(kThreads, 1) dwsep_tc_kernel(const DwParams p)
       int never = 0;
       mbar_wait_bounded(mma_done, 0, p.ctl, &never);
     }
+  } else if (warp == kLoadWarp) {
+    // ------------------------------------------------------------ row loader
+    if (lane == 0) {
+      Ring rr;
+      uint32_t issued = 0;
+      for (int u = blockIdx.x; u < p.units && !*abort_flag; u += gridDim.x) {
+        const int hr = u % p.HR;
+        const int wb = (u / p.HR) % p.WB;
+        const int n = u / (p.HR * p.WB);
+        const int h0 = hr * p.R, h1 = min(p.H, h0 + p.R);
+        for (int r = h0 - 1; r <= h1; ++r) {
+          if (!wait_fast(&row_empty[rr.idx], rr.phase ^ 1u, p.ctl, abort_flag)) goto loader_done;
+          mbar_arrive_expect_tx(&row_full[rr.idx], p.row_bytes);
+          tma_load_3d(smem_rows + (size_t)rr.idx * p.row_bytes, &xmap, wb * kTile - kHalo, r, n * C, &row_full[rr.idx]);
+          rr.next(kRowSlots);
+          ++issued;
+        }
+      }
+    loader_done:
+      if (*abort_flag) {
+        // Let every copy still in flight land before the CTA can exit.
+        Ring back = rr;
+        const uint32_t outstanding = min(issued, (uint32_t)kRowSlots);
+        for (uint32_t i = 0; i < outstanding; ++i) {
+          if (back.idx == 0) {
+            back.idx = kRowSlots - 1;
+            back.phase ^= 1u;
+          } else {
+            --back.idx;
+          }
+          int never = 0;
+          mbar_wait_bounded(&row_full[back.idx], back.phase, p.ctl, &never);
+        }
+      }
+    }
   } else if (warp < kEpiWarp0) {
     // ------------------------------------------------------------ depthwise
-    const int wd = warp - kDwWarp0;  // 0..7
-    const int groups = C >> 2;
+    const int q = warp & 3;                        // TMEM lane quadrant = pixels 32q .. 32q+31
+    const int half = (warp - kDwWarp0) >> 2;       // which half of the channels
+    const int px = q * 32 + lane;
+    const int cper = C >> 1;                       // channels per warp (a multiple of 4)
+    const int cbeg = half * cper;
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     Ring ra;
+    uint32_t rseq = 0;                             // rows consumed before this unit
     for (int u = blockIdx.x; u < p.units && !*abort_flag; u += gridDim.x) {
       const int hr = u % p.HR;
-      const int wb = (u / p.HR) % p.WB;
-      const int n = u / (p.HR * p.WB);
-      const int w0 = wb * kTile;
-      const int h0 = hr * kRows, h1 = min(p.H, h0 + kRows);
+      const int h0 = hr * p.R, h1 = min(p.H, h0 + p.R);
       for (int h = h0; h < h1; ++h) {
+        // Rows h-1, h, h+1 are row numbers s, s+1, s+2 of this CTA's load sequence.
+        const uint32_t s = rseq + (uint32_t)(h - h0);
+        for (uint32_t k = (h == h0 ? 0u : 2u); k < 3u; ++k) {
+          const uint32_t sk = s + k;
+          if (!warp_wait(&row_full[sk % kRowSlots], (sk / kRowSlots) & 1u, p.ctl, abort_flag)) goto dw_done;
+        }
         if (!warp_wait(&a_empty[ra.idx], ra.phase ^ 1u, p.ctl, abort_flag)) goto dw_done;
-        const uint32_t hi_base = smem_addr(smem_a) + ra.idx * p.a_stage_bytes;
-        const uint32_t lo_base = hi_base + p.a_half_bytes;
-        // Ask L2 now for the row the next tile reads first (h + 2), so its loads hit
-        // L2 instead of waiting on HBM: one 512-byte bulk prefetch per channel.
-        if (p.prefetch && h + 2 < p.H && lane < 8 && w0 + kTile <= p.W) {
-          const int g = wd + 8 * (lane >> 2);
-          if (g < groups) {
-            const float* src = p.x + ((size_t)n * C + g * 4 + (lane & 3)) * HW + (size_t)(h + 2) * p.W + w0;
-            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"((uint32_t)kTile * 4u)
-                         : "memory");
-          }
-        }
-        for (int g = wd; g < groups; g += 8) {
-          // All 12 rows (4 channels x 3 image rows) of the group are loaded first so
-          // their latencies overlap; rows outside the image read as zeros (padding).
-          // edge[c][dr]: lane 0 holds pixel w0 - 1 and lane 31 pixel w0 + 128 (one load
-          // instruction for both ends of the row segment; other lanes hold zero).
-          float v[4][3][4], edge[4][3];
-          const bool edge_lane = (lane == 0) ? (w0 > 0) : (lane == 31 && w0 + kTile < p.W);
-          const int edge_off = (lane == 0) ? -1 : kTile;
+        tc_fence_after();
+        const float* rows[3];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const float* xc = p.x + ((size_t)n * C + g * 4 + c) * HW;
+        for (int dr = 0; dr < 3; ++dr)
+          rows[dr] = reinterpret_cast<const float*>(smem_rows + (size_t)((s + dr) % kRowSlots) * p.row_bytes) +
+                     px + kHalo;
+        const uint32_t a_hi = tmem_base + lane_off + (uint32_t)kACol0 + ra.idx * (uint32_t)(2 * C);
+        for (int c0 = cbeg; c0 < cbeg + cper; c0 += 4) {
+          float v[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int ch = c0 + j;
+            float a = 0.0f;
 #pragma unroll
             for (int dr = 0; dr < 3; ++dr) {
-              const int hh = h + dr - 1;
-              const bool rv = (hh >= 0 && hh < p.H);
-              const float* row = xc + (size_t)(rv ? hh : 0) * p.W + w0;
-#pragma unroll
-              for (int k = 0; k < 4; ++k)
-                v[c][dr][k] = (rv && w0 + lane + 32 * k < p.W) ? __ldg(row + lane + 32 * k) : 0.0f;
-              edge[c][dr] = (rv && edge_lane) ? __ldg(row + edge_off) : 0.0f;
+              const float4 kw = *reinterpret_cast<const float4*>(s_wdw + ch * 12 + dr * 4);
+              const float* rw = rows[dr] + ch * kBoxW;
+              a = fmaf(kw.x, rw[-1], fmaf(kw.y, rw[0], fmaf(kw.z, rw[1], a)));
             }
+            v[j] = a;
           }
-          float acc[4][4];
+          float hi[4], lo[4];
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) acc[k][c] = 0.0f;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int ch = g * 4 + c;
-#pragma unroll
-            for (int dr = 0; dr < 3; ++dr) {
-              const float k0 = s_wdw[ch * 9 + dr * 3 + 0];
-              const float k1 = s_wdw[ch * 9 + dr * 3 + 1];
-              const float k2 = s_wdw[ch * 9 + dr * 3 + 2];
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                // One rotate per direction: lane 31 offers the last pixel of the previous
-                // 32-pixel chunk (or the left edge) for lane 0's left neighbour, and lane 0
-                // offers the first pixel of the next chunk (or the right edge) for lane 31.
-                const float x0 = v[c][dr][k];
-                // Edge pixels: lane 0's left end (held by lane 0) and lane 31's right end
-                // (held by lane 31) are used by the same lane, so they bypass the shuffle.
-                const float lsrc = (lane == 31) ? (k > 0 ? v[c][dr][k > 0 ? k - 1 : 0] : 0.0f) : x0;
-                const float rsrc = (lane == 0) ? (k < 3 ? v[c][dr][k < 3 ? k + 1 : 3] : 0.0f) : x0;
-                float left = __shfl_sync(0xffffffffu, lsrc, (lane + 31) & 31);
-                float right = __shfl_sync(0xffffffffu, rsrc, (lane + 1) & 31);
-                if (k == 0 && lane == 0) left = edge[c][dr];
-                if (k == 3 && lane == 31) right = edge[c][dr];
-                acc[k][c] = fmaf(k0, left, fmaf(k1, x0, fmaf(k2, right, acc[k][c])));
-              }
-            }
-          }
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t off = (uint32_t)(g * kTile + lane + 32 * k) * 16u;
-            float hi[4], lo[4];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) split_tf32(acc[k][c], hi[c], lo[c]);
-            st_shared_v4(hi_base + off, hi[0], hi[1], hi[2], hi[3]);
-            st_shared_v4(lo_base + off, lo[0], lo[1], lo[2], lo[3]);
+          for (int j = 0; j < 4; ++j) split_tf32(v[j], hi[j], lo[j]);
+          tmem_st4(a_hi + (uint32_t)c0, hi[0], hi[1], hi[2], hi[3]);
+          tmem_st4(a_hi + (uint32_t)(C + c0), lo[0], lo[1], lo[2], lo[3]);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&a_full[ra.idx]);
+          // Row h-1 is no longer needed; at the strip's end neither are rows h and h+1.
+          mbar_arrive(&row_empty[s % kRowSlots]);
+          if (h == h1 - 1) {
+            mbar_arrive(&row_empty[(s + 1) % kRowSlots]);
+            mbar_arrive(&row_empty[(s + 2) % kRowSlots]);
           }
         }
-        fence_proxy_async_smem();
-        mbar_arrive(&a_full[ra.idx]);
         ra.next(2);
       }
+      rseq += (uint32_t)(h1 - h0 + 2);
     }
   dw_done:;
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quadrant
     const int px = q * 32 + lane;
+    const int HW = p.H * p.W;
     Ring racc;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
@@ -292,21 +343,19 @@ __global__ void __launch_bounds__(kThreads, 1) dwsep_tc_kernel(const DwParams p)
       const int wb = (u / p.HR) % p.WB;
       const int n = u / (p.HR * p.WB);
       const int w = wb * kTile + px;
-      const int h0 = hr * kRows, h1 = min(p.H, h0 + kRows);
+      const int h0 = hr * p.R, h1 = min(p.H, h0 + p.R);
       for (int h = h0; h < h1; ++h) {
         if (!(ok = warp_wait(&acc_full[racc.idx], racc.phase, p.ctl, abort_flag))) break;
         tc_fence_after();
-        const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + racc.idx * (uint32_t)(2 * Cout);
+        const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + racc.idx * (uint32_t)Cout;
         float* yb = p.y + (size_t)n * Cout * HW + (size_t)h * p.W + w;
         for (int c0 = 0; c0 < Cout; c0 += 16) {
-          float v[16], v2[16];
+          float v[16];
           tmem_ld16(tb + c0, v);
-          tmem_ld16(tb + Cout + c0, v2);
           tmem_wait_ld();
           if (w < p.W) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              yb[(size_t)(c0 + j) * HW] = v[j] + v2[j] + (p.bias ? __ldg(&p.bias[c0 + j]) : 0.0f);
+            for (int j = 0; j < 16; ++j) yb[(size_t)(c0 + j) * HW] = v[j] + (p.bias ? __ldg(&p.bias[c0 + j]) : 0.0f);
           }
         }
         tc_fence_before();
@@ -318,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1) dwsep_tc_kernel(const DwParams p)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == kMmaWarp) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
@@ -344,22 +393,32 @@ DwPlan make_dw_plan(int N, int C, int H, int W, int Cout) {
     pl.why = "Cout must be a multiple of 16 and at most 128";
     return pl;
   }
+  if (W % 4 != 0) {
+    pl.why = "W must be a multiple of 4 (rows are copied as 16-byte aligned segments)";
+    return pl;
+  }
+  if ((long long)N * C > 0x7fffffffLL || (long long)H * W > 0x7fffffffLL) {
+    pl.why = "tensor too large";
+    return pl;
+  }
   p.N = N; p.C = C; p.H = H; p.W = W; p.Cout = Cout;
   p.WB = (W + kTile - 1) / kTile;
-  p.HR = (H + kRows - 1) / kRows;
+  // Strips of R rows: each strip re-reads two halo rows, longer strips fill the grid
+  // less evenly; 16 rows balance the two for the large images this path is for.
+  p.R = std::min(H, 16);
+  p.HR = (H + p.R - 1) / p.R;
   const long long units = (long long)N * p.WB * p.HR;
   if (units > 0x7fffffffLL) {
     pl.why = "too many tiles";
     return pl;
   }
   p.units = (int)units;
-  p.a_half_bytes = (uint32_t)(C / 4) * kTile * 16u;
-  p.a_stage_bytes = 2 * p.a_half_bytes;
-  p.off_b = 2 * p.a_stage_bytes;
+  p.row_bytes = (uint32_t)C * kBoxW * 4u;
   const uint32_t b_bytes = (uint32_t)(C / 8) * 2u * (2u * Cout) * 16u;
-  p.off_wdw = p.off_b + b_bytes;
-  p.off_bar = (p.off_wdw + (uint32_t)C * 9u * 4u + 127) / 128 * 128;
-  pl.smem = p.off_bar + 16 * 8;
+  p.off_wdw = b_bytes;
+  p.off_rows = (p.off_wdw + (uint32_t)C * 12u * 4u + 1023) / 1024 * 1024;
+  p.off_bar = p.off_rows + kRowSlots * p.row_bytes;
+  pl.smem = p.off_bar + 32 * 8;
   if (pl.smem + 2048 > (size_t)(227 * 1024)) {
     pl.why = "does not fit in shared memory";
     return pl;
@@ -369,10 +428,26 @@ DwPlan make_dw_plan(int N, int C, int H, int W, int Cout) {
   return pl;
 }
 
+// The driver's tensor-map encoder, looked up once through the runtime (no link-time
+// dependency on the driver library).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
 }  // namespace
 
 const char* dwsep_tc_unsupported_reason(int N, int C, int H, int W, int Cout) {
-  static thread_local char buf[128];
+  static thread_local char buf[160];
   DwPlan pl = make_dw_plan(N, C, H, W, Cout);
   if (pl.ok) return "";
   snprintf(buf, sizeof(buf), "%s", pl.why);
@@ -384,19 +459,34 @@ int dwsep_tc_launch(const DwsepArgs& a) {
   if (sms <= 0) return fail(IG3_ERR_CUDA, "dwsep TC path: cannot query the SM count");
   DwPlan pl = make_dw_plan(a.N, a.C, a.H, a.W, a.Cout);
   if (!pl.ok) return fail(IG3_ERR_UNSUPPORTED, "dwsep TC path: %s", pl.why);
+  if (reinterpret_cast<uintptr_t>(a.x) % 16 != 0)
+    return fail(IG3_ERR_UNSUPPORTED, "dwsep TC path: x must be 16-byte aligned");
   DwParams p = pl.prm;
-  p.x = a.x;
   p.w_dw = a.w_dw;
   p.w_pw = a.w_pw;
   p.bias = a.b;
   p.y = a.y;
-  p.prefetch = (a.W % 4 == 0) && (reinterpret_cast<uintptr_t>(a.x) % 16 == 0);
   p.ctl = wait_ctl();
   if (!p.ctl.status) return fail(IG3_ERR_CUDA, "dwsep TC path: device status word unavailable");
+
+  // x as a 3-D tensor [N*C][H][W] of floats; the box is one row of kBoxW pixels of all
+  // C channels of one image.
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return fail(IG3_ERR_CUDA, "dwsep TC path: cuTensorMapEncodeTiled is not available");
+  CUtensorMap xmap;
+  const cuuint64_t dims[3] = {(cuuint64_t)a.W, (cuuint64_t)a.H, (cuuint64_t)a.N * (cuuint64_t)a.C};
+  const cuuint64_t strides[2] = {(cuuint64_t)a.W * 4u, (cuuint64_t)a.H * (cuuint64_t)a.W * 4u};
+  const cuuint32_t box[3] = {(cuuint32_t)kBoxW, 1u, (cuuint32_t)a.C};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUresult r = encode(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(a.x), dims, strides, box,
+                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(IG3_ERR_CUDA, "dwsep TC path: tensor map encoding failed (%d)", (int)r);
+
   cudaError_t e = cudaFuncSetAttribute(dwsep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
   if (e != cudaSuccess) return cuda_status(e, "dwsep TC: set shared memory size");
   const int grid = std::min(p.units, sms);
-  dwsep_tc_kernel<<<grid, kThreads, pl.smem, a.stream>>>(p);
+  dwsep_tc_kernel<<<grid, kThreads, pl.smem, a.stream>>>(p, xmap);
   return count_launch(cuda_status(cudaGetLastError(), "dwsep TC kernel launch"));
 }
 
