@@ -16,9 +16,13 @@
 //               rows or pixels outside the image come back as zeros, which is the
 //               padding;
 //   warps 2-9   depthwise: lane = pixel (TMEM lane = GEMM row), two warps per TMEM
-//               lane quadrant, each taking half of the channels: nine shared-memory
-//               reads and FMAs per (pixel, channel), the sums split into tf32 hi/lo
-//               and written to tensor memory as the GEMM's A operand;
+//               lane quadrant, each taking half of the channels.  A sliding
+//               window over rows: each staged input row is read once (three values
+//               per pixel and channel) and feeds the three output rows it belongs to
+//               (kernel rows 2, 1, 0 of output rows r-1, r, r+1), whose partial sums
+//               the lane keeps in registers; when row r arrives output row r-1 is
+//               complete, split into tf32 hi/lo and written to tensor memory as the
+//               GEMM's A operand;
 //   warps 10-13 epilogue: tcgen05.ld of a double-buffered accumulator, + bias, one
 //               128-byte line per warp store.
 // Tensor memory: accumulators at columns [0, 2*Cout), A tiles (hi | lo, C columns
@@ -40,10 +44,10 @@
 namespace ig3 {
 namespace {
 
-constexpr int kThreads = 448;
 constexpr int kMmaWarp = 0, kLoadWarp = 1;
-constexpr int kDwWarp0 = 2, kDwWarps = 8;
-constexpr int kEpiWarp0 = 10, kEpiThreads = 128;
+constexpr int kDwWarp0 = 2, kDwWarps = 8;    // two per TMEM lane quadrant
+constexpr int kEpiWarp0 = kDwWarp0 + kDwWarps, kEpiThreads = 128;
+constexpr int kThreads = 32 * kEpiWarp0 + kEpiThreads;
 constexpr int kTile = 128;      // pixels per tile
 constexpr int kHalo = 4;        // staged columns on each side (keeps the copy 16-byte aligned)
 constexpr int kBoxW = kTile + 2 * kHalo;
@@ -151,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_abort = 0;
     for (int i = 0; i < kRowSlots; ++i) {
       mbar_init(&row_full[i], 1);
-      mbar_init(&row_empty[i], kDwWarps);
+      mbar_init(&row_empty[i], kDwWarps);  // each depthwise warp releases a row once read
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&a_full[i], kDwWarps);
@@ -271,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;                        // TMEM lane quadrant = pixels 32q .. 32q+31
     const int half = (warp - kDwWarp0) >> 2;       // which half of the channels
     const int px = q * 32 + lane;
-    const int cper = C >> 1;                       // channels per warp (a multiple of 4)
+    const int cper = C >> 1;                       // channels per warp (a multiple of 8, <= 32)
     const int cbeg = half * cper;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     Ring ra;
@@ -279,54 +283,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int u = blockIdx.x; u < p.units && !*abort_flag; u += gridDim.x) {
       const int hr = u % p.HR;
       const int h0 = hr * p.R, h1 = min(p.H, h0 + p.R);
-      for (int h = h0; h < h1; ++h) {
-        // Rows h-1, h, h+1 are row numbers s, s+1, s+2 of this CTA's load sequence.
-        const uint32_t s = rseq + (uint32_t)(h - h0);
-        for (uint32_t k = (h == h0 ? 0u : 2u); k < 3u; ++k) {
-          const uint32_t sk = s + k;
-          if (!warp_wait(&row_full[sk % kRowSlots], (sk / kRowSlots) & 1u, p.ctl, abort_flag)) goto dw_done;
-        }
-        if (!warp_wait(&a_empty[ra.idx], ra.phase ^ 1u, p.ctl, abort_flag)) goto dw_done;
-        tc_fence_after();
-        const float* rows[3];
+      // acc1[c]: output row r-1 so far (kernel rows 0, 1); acc2[c]: output row r (row 0).
+      float acc1[32], acc2[32];
 #pragma unroll
-        for (int dr = 0; dr < 3; ++dr)
-          rows[dr] = reinterpret_cast<const float*>(smem_rows + (size_t)((s + dr) % kRowSlots) * p.row_bytes) +
-                     px + kHalo;
+      for (int c = 0; c < 32; ++c) acc1[c] = acc2[c] = 0.0f;
+      for (int r = h0 - 1; r <= h1; ++r) {
+        const uint32_t sr = rseq + (uint32_t)(r - (h0 - 1));
+        if (!warp_wait(&row_full[sr % kRowSlots], (sr / kRowSlots) & 1u, p.ctl, abort_flag)) goto dw_done;
+        const bool emit = (r - 1 >= h0);           // output row r-1 completes with this row
+        if (emit) {
+          if (!warp_wait(&a_empty[ra.idx], ra.phase ^ 1u, p.ctl, abort_flag)) goto dw_done;
+          tc_fence_after();
+        }
+        const float* row = reinterpret_cast<const float*>(smem_rows + (size_t)(sr % kRowSlots) * p.row_bytes) +
+                           (size_t)cbeg * kBoxW + px + kHalo;
         const uint32_t a_hi = tmem_base + lane_off + (uint32_t)kACol0 + ra.idx * (uint32_t)(2 * C);
-        for (int c0 = cbeg; c0 < cbeg + cper; c0 += 4) {
-          float v[4];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int ch = c0 + j;
-            float a = 0.0f;
+        for (int cg = 0; cg < 32; cg += 4) {
+          if (cg < cper) {
+            float fin[4];
 #pragma unroll
-            for (int dr = 0; dr < 3; ++dr) {
-              const float4 kw = *reinterpret_cast<const float4*>(s_wdw + ch * 12 + dr * 4);
-              const float* rw = rows[dr] + ch * kBoxW;
-              a = fmaf(kw.x, rw[-1], fmaf(kw.y, rw[0], fmaf(kw.z, rw[1], a)));
+            for (int j = 0; j < 4; ++j) {
+              const int c = cg + j;
+              const float* rw = row + c * kBoxW;
+              const float xl = rw[-1], xc = rw[0], xr = rw[1];
+              const float* kw = s_wdw + (cbeg + c) * 12;
+              const float4 k0 = *reinterpret_cast<const float4*>(kw);      // kernel row 0
+              const float4 k1 = *reinterpret_cast<const float4*>(kw + 4);  // kernel row 1
+              const float4 k2 = *reinterpret_cast<const float4*>(kw + 8);  // kernel row 2
+              fin[j] = fmaf(k2.x, xl, fmaf(k2.y, xc, fmaf(k2.z, xr, acc1[c])));
+              acc1[c] = fmaf(k1.x, xl, fmaf(k1.y, xc, fmaf(k1.z, xr, acc2[c])));
+              acc2[c] = fmaf(k0.x, xl, fmaf(k0.y, xc, k0.z * xr));
             }
-            v[j] = a;
-          }
-          float hi[4], lo[4];
+            if (emit) {
+              float hi[4], lo[4];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) split_tf32(v[j], hi[j], lo[j]);
-          tmem_st4(a_hi + (uint32_t)c0, hi[0], hi[1], hi[2], hi[3]);
-          tmem_st4(a_hi + (uint32_t)(C + c0), lo[0], lo[1], lo[2], lo[3]);
+              for (int j = 0; j < 4; ++j) split_tf32(fin[j], hi[j], lo[j]);
+              tmem_st4(a_hi + (uint32_t)(cbeg + cg), hi[0], hi[1], hi[2], hi[3]);
+              tmem_st4(a_hi + (uint32_t)(C + cbeg + cg), lo[0], lo[1], lo[2], lo[3]);
+            }
+          }
         }
-        tmem_wait_st();
-        tc_fence_before();
+        if (emit) {
+          tmem_wait_st();
+          tc_fence_before();
+        }
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&a_full[ra.idx]);
-          // Row h-1 is no longer needed; at the strip's end neither are rows h and h+1.
-          mbar_arrive(&row_empty[s % kRowSlots]);
-          if (h == h1 - 1) {
-            mbar_arrive(&row_empty[(s + 1) % kRowSlots]);
-            mbar_arrive(&row_empty[(s + 2) % kRowSlots]);
-          }
+          mbar_arrive(&row_empty[sr % kRowSlots]);  // this row is not read again
+          if (emit) mbar_arrive(&a_full[ra.idx]);
         }
-        ra.next(2);
+        if (emit) ra.next(2);
       }
       rseq += (uint32_t)(h1 - h0 + 2);
     }
@@ -349,13 +356,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + racc.idx * (uint32_t)Cout;
         float* yb = p.y + (size_t)n * Cout * HW + (size_t)h * p.W + w;
-        for (int c0 = 0; c0 < Cout; c0 += 16) {
-          float v[16];
-          tmem_ld16(tb + c0, v);
-          tmem_wait_ld();
-          if (w < p.W) {
+        // 16-column chunks, two register buffers: the load of chunk k+1 is in flight
+        // while chunk k is stored.
+        float va[16], vb[16];
+        tmem_ld16(tb, va);
+        tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) yb[(size_t)(c0 + j) * HW] = v[j] + (p.bias ? __ldg(&p.bias[c0 + j]) : 0.0f);
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          if (c0 < Cout) {
+            if (c0 + 16 < Cout) tmem_ld16(tb + (uint32_t)(c0 + 16), vb);
+            if (w < p.W) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) yb[(size_t)(c0 + j) * HW] = va[j] + (p.bias ? __ldg(&p.bias[c0 + j]) : 0.0f);
+            }
+            tmem_wait_ld();
+          }
+          if (c0 + 16 < Cout) {
+            if (c0 + 32 < Cout) tmem_ld16(tb + (uint32_t)(c0 + 32), va);
+            if (w < p.W) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                yb[(size_t)(c0 + 16 + j) * HW] = vb[j] + (p.bias ? __ldg(&p.bias[c0 + 16 + j]) : 0.0f);
+            }
+            tmem_wait_ld();
           }
         }
         tc_fence_before();
@@ -385,8 +408,8 @@ DwPlan make_dw_plan(int N, int C, int H, int W, int Cout) {
   DwPlan pl;
   DwParams& p = pl.prm;
   std::memset(&p, 0, sizeof(p));
-  if (C % 8 != 0 || C > 64) {
-    pl.why = "C must be a multiple of 8 and at most 64";
+  if (C % 16 != 0 || C > 64) {
+    pl.why = "C must be a multiple of 16 and at most 64";
     return pl;
   }
   if (Cout % 16 != 0 || Cout > 128) {
