@@ -404,7 +404,7 @@ struct DwPlan {
   size_t smem = 0;
 };
 
-DwPlan make_dw_plan(int N, int C, int H, int W, int Cout) {
+DwPlan make_dw_plan(int N, int C, int H, int W, int Cout, int sms = 148) {
   DwPlan pl;
   DwParams& p = pl.prm;
   std::memset(&p, 0, sizeof(p));
@@ -426,9 +426,19 @@ DwPlan make_dw_plan(int N, int C, int H, int W, int Cout) {
   }
   p.N = N; p.C = C; p.H = H; p.W = W; p.Cout = Cout;
   p.WB = (W + kTile - 1) / kTile;
-  // Strips of R rows: each strip re-reads two halo rows, longer strips fill the grid
-  // less evenly; 16 rows balance the two for the large images this path is for.
-  p.R = std::min(H, 16);
+  // Strips of R rows: each strip reads R + 2 rows, and the persistent grid takes
+  // ceil(units / SMs) rounds of strips; pick R minimising rounds x (R + 2).
+  long long best = -1;
+  for (int R : {8, 16, 32, 64}) {
+    const int r = std::min(H, R);
+    const long long u = (long long)N * p.WB * ((H + r - 1) / r);
+    const long long cost = (u + sms - 1) / sms * (r + 2);
+    if (best < 0 || cost < best) {
+      best = cost;
+      p.R = r;
+    }
+    if (r == H) break;
+  }
   p.HR = (H + p.R - 1) / p.R;
   const long long units = (long long)N * p.WB * p.HR;
   if (units > 0x7fffffffLL) {
@@ -480,7 +490,7 @@ const char* dwsep_tc_unsupported_reason(int N, int C, int H, int W, int Cout) {
 int dwsep_tc_launch(const DwsepArgs& a) {
   const int sms = num_sms();
   if (sms <= 0) return fail(IG3_ERR_CUDA, "dwsep TC path: cannot query the SM count");
-  DwPlan pl = make_dw_plan(a.N, a.C, a.H, a.W, a.Cout);
+  DwPlan pl = make_dw_plan(a.N, a.C, a.H, a.W, a.Cout, sms);
   if (!pl.ok) return fail(IG3_ERR_UNSUPPORTED, "dwsep TC path: %s", pl.why);
   if (reinterpret_cast<uintptr_t>(a.x) % 16 != 0)
     return fail(IG3_ERR_UNSUPPORTED, "dwsep TC path: x must be 16-byte aligned");
