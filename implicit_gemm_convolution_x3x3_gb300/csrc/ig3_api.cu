@@ -233,6 +233,10 @@ int dwsep_conv2d(const float* x, int N, int C, int H, int W, const float* w_dw, 
     return fail(IG3_ERR_INVALID_ARG, "dwsep_conv2d: x, w_dw, w_pw and y must not be NULL");
   if (!current_device()) return fail(IG3_ERR_CUDA, "dwsep_conv2d: device set-up failed");
   DwsepArgs a{x, N, C, H, W, w_dw, w_pw, Cout, b, y, static_cast<cudaStream_t>(stream)};
+  // The tensor-core kernel copies 16-byte aligned row segments; a misaligned x goes to
+  // the FMA kernel when the caller left the choice to the library.
+  if (p == IG3_PATH_TC && path == IG3_PATH_AUTO && reinterpret_cast<uintptr_t>(x) % 16 != 0)
+    return dwsep_fma_launch(a);
   return p == IG3_PATH_TC ? dwsep_tc_launch(a) : dwsep_fma_launch(a);
 }
 

@@ -143,8 +143,9 @@ int conv3d_fused_noalloc(const float* x, int N, int Cin, int D, int H, int W,
  *   x    [N][C][H][W]      w_dw [C][1][3][3]      w_pw [Cout][C][1][1]
  *   b    [Cout] or NULL    (a combined bias, sum_c w_pw[o,c] * b_dw[c] + b_pw[o])
  *   y    [N][Cout][H][W]
- * IG3_PATH_TC requires C a multiple of 8 and <= 64, and Cout a multiple of 16 and
- * <= 128 (else IG3_ERR_UNSUPPORTED).
+ * IG3_PATH_TC requires C a multiple of 16 and <= 64, Cout a multiple of 16 and <= 128,
+ * W a multiple of 4 and x 16-byte aligned (else IG3_ERR_UNSUPPORTED); with
+ * IG3_PATH_AUTO a misaligned x takes the FMA path.
  */
 int dwsep_conv2d(const float* x, int N, int C, int H, int W,
                  const float* w_dw, const float* w_pw, int Cout, const float* b,

@@ -43,6 +43,9 @@ CASES = [
     (1, 3, 5, 5, 5, True),        # odd channels
     (1, 8, 1, 1, 16, False),      # 1x1 image: only the centre tap sees data
     (2, 8, 2, 4, 16, True),
+    (1, 16, 1, 8, 16, False),     # H = 1: both halo rows come from outside the image
+    (2, 16, 37, 132, 16, False),  # W = 132: a 4-pixel second segment; strips end mid-image
+    (1, 48, 70, 260, 112, True),  # three segments, several strips, Cout 112
 ]
 
 
@@ -69,3 +72,24 @@ def test_dwsep_full_size_sampled(ig3):
     assert bool(torch.isfinite(out).all())
     del x, w_dw, w_pw, out
     torch.cuda.empty_cache()
+
+
+def test_dwsep_misaligned_input(ig3):
+    """x 4 bytes off a 16-byte boundary: the tensor-core kernel needs 16-byte aligned
+    rows, so an explicit request is refused and the automatic choice takes the FMA
+    kernel; either way nothing runs on the wrong data."""
+    N, C, H, W, Cout = 1, 64, 64, 128, 128      # large enough for the automatic choice to pick TC
+    assert ig3.dwsep_conv2d_select_path(N, C, H, W, Cout, "auto") == "tc"
+    wl = si.dwsep_workload("t", N, C, H, W, Cout, seed=3100, with_bias=False)
+    t = wl.generate_all()
+    ref = oracle.dwsep(t["x"], t["w_dw"], t["w_pw"], None)
+    buf = torch.empty(t["x"].size + 1, dtype=torch.float32, device="cuda")
+    x = buf[1:].view(t["x"].shape)
+    x.copy_(torch.from_numpy(t["x"]))
+    assert x.data_ptr() % 16 != 0
+    w_dw = to_dev(t["w_dw"]); w_pw = to_dev(t["w_pw"])
+    with pytest.raises(ig3.Ig3Error):
+        ig3.dwsep_conv2d(x, w_dw, w_pw, None, path="tc")
+    out = ig3.dwsep_conv2d(x, w_dw, w_pw, None)
+    assert ig3.ig3_last_device_status() == 0
+    assert_close(out.cpu().numpy(), ref, "misaligned auto")
