@@ -227,12 +227,18 @@ Plan make_plan_uncached(int N, int Cin, int D, int H, int W, int Cout, int epi, 
       const double c_full = unit_cycles(kdm, hl, P, Cout, KS, nchunks, T, res, npos, xs > 0);
       const double c_last = unit_cycles(kdm, hl, last, Cout, KS, nchunks, T, res, npos, xs > 0);
       // Round-robin over the grid: CTA c takes units c, c + grid, ...; a unit is
-      // the last split iff u % S == S - 1.
+      // the last split iff u % S == S - 1.  Simulated exactly up to 65536 units; past
+      // that, bounded by the rounds times the dearer unit (the difference is small
+      // once every CTA takes many units).
       double worst = 0.0;
-      for (int c = 0; c < grid; ++c) {
-        double t = 0.0;
-        for (long long u = c; u < units; u += grid) t += (u % S == S - 1) ? c_last : c_full;
-        worst = std::max(worst, t);
+      if (units <= 65536) {
+        for (int c = 0; c < grid; ++c) {
+          double t = 0.0;
+          for (long long u = c; u < units; u += grid) t += (u % S == S - 1) ? c_last : c_full;
+          worst = std::max(worst, t);
+        }
+      } else {
+        worst = (double)((units + grid - 1) / grid) * std::max(c_full, c_last);
       }
       if (worst < best * (1.0 - 1e-9)) {
         best = worst;
