@@ -356,27 +356,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + racc.idx * (uint32_t)Cout;
         float* yb = p.y + (size_t)n * Cout * HW + (size_t)h * p.W + w;
-        // 16-column chunks, two register buffers: the load of chunk k+1 is in flight
-        // while chunk k is stored.
-        float va[16], vb[16];
-        tmem_ld16(tb, va);
+        // 32-column chunks, two register buffers: the load of chunk k+1 is in flight
+        // while chunk k is stored.  When Cout is an odd multiple of 16 the last load
+        // also reads 16 columns past the accumulator (inside the allocation); those
+        // values are not stored.
+        float va[32], vb[32];
+        tmem_ld32(tb, va);
         tmem_wait_ld();
 #pragma unroll
-        for (int c0 = 0; c0 < 128; c0 += 32) {
+        for (int c0 = 0; c0 < 128; c0 += 64) {
           if (c0 < Cout) {
-            if (c0 + 16 < Cout) tmem_ld16(tb + (uint32_t)(c0 + 16), vb);
+            if (c0 + 32 < Cout) tmem_ld32(tb + (uint32_t)(c0 + 32), vb);
             if (w < p.W) {
 #pragma unroll
-              for (int j = 0; j < 16; ++j) yb[(size_t)(c0 + j) * HW] = va[j] + (p.bias ? __ldg(&p.bias[c0 + j]) : 0.0f);
+              for (int j = 0; j < 32; ++j)
+                if (j < 16 || c0 + 32 <= Cout)
+                  yb[(size_t)(c0 + j) * HW] = va[j] + (p.bias ? __ldg(&p.bias[c0 + j]) : 0.0f);
             }
             tmem_wait_ld();
           }
-          if (c0 + 16 < Cout) {
-            if (c0 + 32 < Cout) tmem_ld16(tb + (uint32_t)(c0 + 32), va);
+          if (c0 + 32 < Cout) {
+            if (c0 + 64 < Cout) tmem_ld32(tb + (uint32_t)(c0 + 64), va);
             if (w < p.W) {
 #pragma unroll
-              for (int j = 0; j < 16; ++j)
-                yb[(size_t)(c0 + 16 + j) * HW] = vb[j] + (p.bias ? __ldg(&p.bias[c0 + 16 + j]) : 0.0f);
+              for (int j = 0; j < 32; ++j)
+                if (j < 16 || c0 + 64 <= Cout)
+                  yb[(size_t)(c0 + 32 + j) * HW] = vb[j] + (p.bias ? __ldg(&p.bias[c0 + 32 + j]) : 0.0f);
             }
             tmem_wait_ld();
           }
