@@ -23,15 +23,25 @@
 // three products is one MMA into the same accumulator columns.
 //
 // Window MMAs.  Input plane d feeds output planes d-2, d-1, d through the kd = 2, 1, 0
-// weights.  One thread can issue a tcgen05.mma only every ~46 cycles, so small MMAs
-// leave the tensor pipe idle; instead the accumulators of consecutive output planes
-// sit in adjacent TMEM slots (Cout columns each) and the weights of one (kh, kw) tap
-// are stored with rows [kd=2 | kd=1 | kd=0], so ONE MMA with N = 3*Cout applies all
-// three kd of an input plane (KDM 3, Cout <= 80).  A unit's P output planes use slots
-// 0..P-1, so the window never wraps; planes at the ends of a unit use the sub-window
-// of the kd that fall inside it.  Every MMA accumulates: the slots start at zero and
-// the epilogue zeroes each slot after reading it.  For Cout > 80 (3*Cout > 256, the
-// largest N) each kd is its own MMA (KDM 1) and the slots form a ring.
+// weights.  An M = 128, K = 8 tf32 MMA reads its whole A tile (4 KB) and its B rows
+// (32 B per column) from shared memory at ~128 B per cycle, so below N ~ 128 the
+// operand reads, not the arithmetic, set its cost (measured alone: 48 cycles at
+// N = 48, 58 at 96, 66 at 128, 98 at 192).  Small MMAs are therefore merged: the
+// accumulators of consecutive output planes sit in adjacent TMEM slots (Cout columns
+// each) and the weights of one (kh, kw) tap are stored with rows [kd=2 | kd=1 |
+// kd=0], so ONE MMA with N = 3*Cout applies all three kd of an input plane (KDM 3,
+// Cout <= 80).  A unit's P output planes use slots 0..P-1, so the window never wraps;
+// planes at the ends of a unit use the sub-window of the kd that fall inside it.
+// Every MMA accumulates: the slots start at the bias and the epilogue writes the
+// bias back after reading a slot.  For Cout > 80 (3*Cout > 256, the largest N) each
+// kd is its own MMA (KDM 1) and the slots form a ring.
+//
+// Window over kd and kw (KDM 9, Cout 16, not pool-reduce).  The A tile is shifted by
+// kh*W only, and one MMA with N = 9*Cout (three kd x three kw) applies an input
+// plane to three output planes: slot = [kw=0 | kw=1 | kw=2] x Cout, and the
+// epilogue adds block kw of position o + kw into output o (a lane shuffle; across a
+// quadrant boundary, a shared-memory hand-over).  Tiles must hold whole input rows
+// (W divides 128), so the shift never leaves the tile.
 //
 // Data flow (persistent CTAs, one per SM, 512 threads, warp-specialised):
 //   warp 0      weight producer: 1-D bulk copies (TMA) of pre-split K-step blocks from
@@ -80,11 +90,15 @@ using namespace tc;
 //                row range;
 //   KDM 3, HL:   block (khw * KS + ks), rows [hi kd=2 | lo kd=2 | hi kd=1 | lo kd=1 |
 //                hi kd=0 | lo kd=0 | hi kd=2 | 0 | hi kd=1 | 0 | hi kd=0 | 0] x Cout;
+//   KDM 9:       block (kh * KS + ks), rows [hi kd=2 kw=0 | hi kd=2 kw=1 | hi kd=2 kw=2 |
+//                hi kd=1 kw=0 | ... | hi kd=0 kw=2 | lo, the same nine] x Cout;
 //   KDM 1:       block ((kd * 9 + khw) * KS + ks), rows [hi | lo] x Cout.
 // khw = kh * 3 + kw.
-__host__ __device__ int blob_rows(int kdm, int hl, int Cout) { return (kdm == 3 ? (hl ? 12 : 6) : 2) * Cout; }
+__host__ __device__ int blob_rows(int kdm, int hl, int Cout) {
+  return (kdm == 9 ? 18 : kdm == 3 ? (hl ? 12 : 6) : 2) * Cout;
+}
 size_t blob_floats(int kdm, int hl, int KS, int Cout) {
-  return (size_t)(kdm == 3 ? 9 : 27) * KS * 2 * blob_rows(kdm, hl, Cout) * 4;
+  return (size_t)(kdm == 9 ? 3 : kdm == 3 ? 9 : 27) * KS * 2 * blob_rows(kdm, hl, Cout) * 4;
 }
 
 __global__ void conv3d_tc_prep_weights(const float* __restrict__ w, float* __restrict__ blob, int Cin, int Cout,
@@ -109,6 +123,13 @@ __global__ void conv3d_tc_prep_weights(const float* __restrict__ w, float* __res
       zero = (half == 1) && !hi;
       co = rr % Cout;
       tap = kd * 9 + blk;  // blk = khw
+    } else if (kdm == 9) {
+      hi = row < 9 * Cout;
+      const int rr = hi ? row : row - 9 * Cout;
+      const int kd = 2 - rr / (3 * Cout);
+      const int kw = (rr / Cout) % 3;
+      co = rr % Cout;
+      tap = kd * 9 + blk * 3 + kw;  // blk = kh
     } else if (kdm == 3) {
       hi = row < 3 * Cout;
       const int rr = hi ? row : row - 3 * Cout;
@@ -145,7 +166,20 @@ int positions_tiles(int OH, int W, int T) { return ((OH * W) + T * 128 - 1) / (T
 // time) and every streamed weight stage ~250 more.  The chunk's input convert runs
 // alongside: ~0.9 cycles per value when the convert warps load x themselves (latency
 // bound), ~0.35 when a bulk-copy loader stages it ahead.
+//
+// KDM 9: three MMAs (one per split product) per (kh, K-step, tile) with N = 3 * nkd *
+// Cout.  At this N an MMA is bound as much by shared-memory reads (A 4 KB + B 32 B
+// per column, at 128 B per cycle) as by its execution, and the input convert's
+// traffic (raw copy in, raw read, hi and lo out) shares the same port.
 double plane_cycles(int kdm, int hl, int nkd, int Cout, int KS, int nchunks, int T, bool res, int npos, bool xstage) {
+  if (kdm == 9) {
+    const double n = 3.0 * nkd * Cout;
+    const double mmas = 3.0 * KS * T * 3.0;
+    const double exec = mmas * (0.5 * n + 5.0) + (res ? 0.0 : 250.0 * 3.0 * nchunks);
+    const double port = (mmas * (4096.0 + 32.0 * n) + npos * 8.0 * KS * 16.0) / 128.0;
+    const double conv = (xstage ? 0.35 : 0.9) * npos * (8.0 * KS);
+    return 1.1 * std::max(std::max(exec, port), conv) + 300.0 * nchunks;
+  }
   const int mmas_per_step = (kdm == 3) ? (hl ? 2 : 3) : 3 * nkd;
   const int n = (kdm == 3) ? nkd * Cout * (hl ? 2 : 1) : Cout;
   const double mmas = 9.0 * KS * T * mmas_per_step;
@@ -180,7 +214,12 @@ Plan make_plan_uncached(int N, int Cin, int D, int H, int W, int Cout, int epi, 
     return pl;
   }
   const int OD = D - 2, OH = H - 2;
-  const int kdm = (3 * Cout <= 256) ? 3 : 1;
+  // Cout 16 with tiles of whole input rows (W divides 128): kw joins kd inside the
+  // MMA's N (the epilogue's shifted sum never crosses a tile).  Not for pool-reduce:
+  // its epilogue, not the MMAs, bounds it, and the shift exchange adds to it.
+  const int kdm = (epi != IG3_EPI_POOL_REDUCE && Cout == 16 && W <= 128 && 128 % W == 0) ? 9
+                  : (3 * Cout <= 256)                                                      ? 3
+                                                                                           : 1;
   const int hl = (kdm == 3 && 6 * Cout <= 256) ? 1 : 0;
   const int ks0 = (Cin + 7) / 8;
   const int step = (epi == IG3_EPI_POOL_REDUCE) ? 2 : 1;
@@ -191,14 +230,15 @@ Plan make_plan_uncached(int N, int Cin, int D, int H, int W, int Cout, int epi, 
     const bool res = v.res != 0;
     const int KS = (ks0 + kss - 1) / kss * kss;
     const int nchunks = KS / kss;
-    const int nslot = std::min(kMaxSlots, kTmemCols / (T * Cout * (hl ? 2 : 1)));
-    if (nslot < (kdm == 3 ? step : 4)) continue;
+    const int nslot = std::min(kMaxSlots, kTmemCols / (T * Cout * (kdm == 9 ? 3 : hl ? 2 : 1)));
+    if (nslot < (kdm != 1 ? step : 4)) continue;
     const int npos = ((T * 128 + 2 * W + 2) + 7) / 8 * 8;
     const uint32_t a_half = (uint32_t)(2 * kss) * npos * 16u;
     const uint32_t a_stage = 2 * a_half;
     const uint32_t blk = (uint32_t)(2 * blob_rows(kdm, hl, Cout) * 16);
     const uint32_t blob = (uint32_t)(blob_floats(kdm, hl, KS, Cout) * 4);
-    const uint32_t epi_bytes = (epi == IG3_EPI_POOL_REDUCE) ? (uint32_t)(2 * 16 * 32 + T * Cout * 32) * 4u : 0u;
+    const uint32_t epi_bytes = ((epi == IG3_EPI_POOL_REDUCE) ? (uint32_t)(2 * 16 * 32 + T * Cout * 32) * 4u : 0u) +
+                               (kdm == 9 ? 2u * 2u * (uint32_t)T * 4u * 24u * 4u : 0u);
     const uint32_t off_b = kAStages * a_stage;
     // 2 KB for static shared memory and alignment; barriers for the largest ring.
     const long long avail = (long long)kSmemLimit - off_b - epi_bytes - 2048 - 128 - 128 -
@@ -216,8 +256,8 @@ Plan make_plan_uncached(int N, int Cin, int D, int H, int W, int Cout, int epi, 
     const long long left = avail - (res ? (long long)blob : (long long)sb * kss * blk);
     int xs = (int)std::min<long long>(kMaxXStages, left / x_stage);
     if (xs < 2) xs = 0;
-    // Planes per unit: with KDM 3 a unit's planes must fit the slots.
-    const int pmax = (kdm == 3) ? std::min(OD, nslot) : OD;
+    // Planes per unit: with KDM 3 and 9 a unit's planes must fit the slots.
+    const int pmax = (kdm != 1) ? std::min(OD, nslot) : OD;
     const int G = positions_tiles(OH, W, T);
     for (int P = pmax - (pmax % step == 0 ? 0 : 1); P >= step; P -= step) {
       const int S = (OD + P - 1) / P;

@@ -33,9 +33,11 @@ struct TcParams {
   int nchunks;   // KS / KSS
   int T;         // position tiles of 128 per unit
   int NPOS;      // positions held per A stage
-  int KDM;       // 3: one MMA spans the kd = 2, 1, 0 accumulators; 1: one MMA per kd
+  int KDM;       // 3: one MMA spans the kd = 2, 1, 0 accumulators; 1: one MMA per kd;
+                 // 9: one MMA spans kd and kw (slot = [kw=0 | kw=1 | kw=2] x Cout, summed
+                 // with a one- and two-position shift in the epilogue)
   int HL;        // KDM 3 only: hi and lo products in separate columns (slot = 2*Cout)
-  int NSLOT;     // accumulator slots per tile, Cout (HL: 2*Cout) columns each
+  int NSLOT;     // accumulator slots per tile, Cout (HL: 2*Cout; KDM 9: 3*Cout) columns each
   int G, S, P;   // tile groups per plane, plane splits, output planes per split
   int units;
   int resident;  // weights loaded once
@@ -78,11 +80,11 @@ static __host__ __device__ __forceinline__ Unit decode_unit(const TcParams& p, i
   return r;
 }
 
-// First accumulator slot of a unit: with KDM 3 every unit starts at slot 0 (its P
-// planes fit in the slots, so a window of adjacent planes never wraps); with KDM 1
+// First accumulator slot of a unit: with KDM 3 and 9 every unit starts at slot 0 (its
+// P planes fit in the slots, so a window of adjacent planes never wraps); with KDM 1
 // the slots form a ring that runs on across units.
 static __host__ __device__ __forceinline__ uint32_t unit_slot0(const TcParams& p, uint32_t plane_seq) {
-  return p.KDM == 3 ? 0u : plane_seq % (uint32_t)p.NSLOT;
+  return p.KDM != 1 ? 0u : plane_seq % (uint32_t)p.NSLOT;
 }
 
 // Slot of the unit's k-th output plane (k >= 0; with KDM 1, k may exceed NSLOT).
@@ -157,11 +159,12 @@ static __device__ __forceinline__ void issue_stage(uint32_t dcol, uint32_t tile_
   }
 }
 
-// All nine (kh, kw) taps of one A chunk against one set of accumulator columns.
-// Streaming weights: one ring stage per tap, waited for, used and released.
-// Resident weights: block (tap_base + khw) * KS + blk0.  Returns false if a wait gave
-// up (the MMAs are still issued, on whatever the buffers hold; the caller stops).
-template <int T, int KSS, bool RES, bool HL>
+// All (kh, kw) taps of one A chunk against one set of accumulator columns: nine, or
+// with NKW = 1 (kw inside the MMA's N) the three kh.  Streaming weights: one ring
+// stage per tap, waited for, used and released.  Resident weights: block
+// (tap_base + kh * NKW + kw) * KS + blk0.  Returns false if a wait gave up (the MMAs
+// are still issued, on whatever the buffers hold; the caller stops).
+template <int T, int KSS, bool RES, bool HL, int NKW>
 static __device__ __forceinline__ bool issue_taps(const TcParams& p, uint32_t dcol, uint32_t tile_cols,
                                                   uint64_t ah0, uint64_t al0, uint64_t bwin, uint32_t lo_u,
                                                   uint32_t ks_u, uint32_t blk_u, uint32_t row_u, uint32_t idesc,
@@ -172,11 +175,11 @@ static __device__ __forceinline__ bool issue_taps(const TcParams& p, uint32_t dc
 #pragma unroll
   for (int kh = 0; kh < 3; ++kh) {
 #pragma unroll
-    for (int kw = 0; kw < 3; ++kw) {
+    for (int kw = 0; kw < NKW; ++kw) {
       const uint64_t tap_u = (uint64_t)((uint32_t)kh * row_u + (uint32_t)kw);
       uint64_t bst;
       if constexpr (RES) {
-        bst = bwin + (uint64_t)((uint32_t)((tap_base + kh * 3 + kw) * p.KS + blk0) * blk_u);
+        bst = bwin + (uint64_t)((uint32_t)((tap_base + kh * NKW + kw) * p.KS + blk0) * blk_u);
       } else {
         if (!wait_fast(&b_full[rb.idx], rb.phase, p.ctl, abort_flag)) good = false;
         tc_fence_after();
@@ -206,6 +209,18 @@ static __device__ __forceinline__ void load_bias16(const float* src, float (&v)[
 
 static __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// bar.sync that also returns the AND of v over the participating threads.
+static __device__ __forceinline__ bool named_bar_and(int id, int count, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\tbar.red.and.pred po, %2, %3, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
 }
 
 static __device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, float b, float c, float d) {
@@ -241,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   volatile int* abort_flag = &s_abort;
-  const uint32_t slot_w = (uint32_t)((HL ? 2 : 1) * p.Cout);  // accumulator columns per slot
+  const uint32_t slot_w = (uint32_t)((KDM == 9 ? 3 : HL ? 2 : 1) * p.Cout);  // accumulator columns per slot
   const uint32_t tile_cols = (uint32_t)p.NSLOT * slot_w;
 
   if (tid < p.Cout) s_bias[tid] = p.bias ? p.bias[tid] : 0.0f;
@@ -320,12 +335,12 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
             const int kd_hi = min(2, d - un.od0), kd_lo = max(0, d - un.od1 + 1);
             for (int ch = 0; ch < p.nchunks; ++ch) {
               // The stages in the order the MMA issuer consumes them: KDM 3, the nine
-              // taps (each block holds all three kd); KDM 1, the valid kd from 2 down,
-              // nine taps each.
-              const int nkd = (KDM == 3) ? 1 : kd_hi - kd_lo + 1;
+              // taps (each block holds all three kd); KDM 9, the three kh (each block
+              // holds all kd and kw); KDM 1, the valid kd from 2 down, nine taps each.
+              const int nkd = (KDM != 1) ? 1 : kd_hi - kd_lo + 1;
               for (int k = 0; k < nkd; ++k) {
-                const int tap_base = (KDM == 3) ? 0 : (kd_hi - k) * 9;
-                for (int khw = 0; khw < 9; ++khw) {
+                const int tap_base = (KDM != 1) ? 0 : (kd_hi - k) * 9;
+                for (int khw = 0; khw < (KDM == 9 ? 3 : 9); ++khw) {
                   if (!wait_fast(&b_empty[rb.idx], rb.phase ^ 1u, p.ctl, abort_flag)) goto producer_done;
                   const int blk = (tap_base + khw) * p.KS + ch * KSS;
                   mbar_arrive_expect_tx(&b_full[rb.idx], stage_bytes);
@@ -362,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
       // Descriptors are formed once and advanced by plain adds in 16-byte units (the
       // start-address field is the low 14 bits), so the issue loop stays a short
       // chain of adds and tcgen05.mma.
-      const uint32_t b_rows = (uint32_t)((KDM == 3 ? (HL ? 12 : 6) : 2) * p.Cout);
+      const uint32_t b_rows = (uint32_t)((KDM == 9 ? 18 : KDM == 3 ? (HL ? 12 : 6) : 2) * p.Cout);
       const uint64_t a_desc0 = umma_desc_noswizzle(smem_addr(smem_a), (uint32_t)p.NPOS * 16u, 128);
       const uint64_t b_desc0 = umma_desc_noswizzle(smem_addr(smem_b), b_rows * 16u, 128);
       const uint32_t a_stage_u = p.a_stage_bytes >> 4, a_half_u = p.a_half_bytes >> 4;
@@ -395,28 +410,29 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
             }
             const uint64_t ah0 = a_desc0 + (uint64_t)(ra.idx * a_stage_u);
             const uint64_t al0 = ah0 + a_half_u;
-            if constexpr (KDM == 3) {
+            if constexpr (KDM != 1) {
               // One window: the accumulators of od = d - kd_hi .. d - kd_lo are adjacent
               // (slots ascend with od), the B rows of kd = kd_hi .. kd_lo too.
               const uint32_t nkd = (uint32_t)(kd_hi - kd_lo + 1);
               const uint32_t dcol = tmem_base + (s0 + (uint32_t)(d - kd_hi - un.od0)) * slot_w;
               const uint32_t idesc = umma_idesc_tf32(128, (int)(nkd * slot_w));
               const uint64_t bwin = b_desc0 + (uint64_t)((uint32_t)(2 - kd_hi) * slot_w);
-              ok = issue_taps<T, KSS, RES, HL>(p, dcol, tile_cols, ah0, al0, bwin, lo_u, ks_u, blk_u, row_u, idesc, 0,
-                                           ch * KSS, b_full, b_empty, rb, abort_flag);
+              ok = issue_taps<T, KSS, RES, HL, (KDM == 9 ? 1 : 3)>(p, dcol, tile_cols, ah0, al0, bwin, lo_u, ks_u, blk_u,
+                                                                   row_u, idesc, 0, ch * KSS, b_full, b_empty, rb,
+                                                                   abort_flag);
             } else {
               for (int kd = kd_hi; ok && kd >= kd_lo; --kd) {
                 const uint32_t dcol = tmem_base + slot_add(p, s0, d - kd - un.od0) * cout;
-                ok = issue_taps<T, KSS, RES, false>(p, dcol, tile_cols, ah0, al0, b_desc0, lo_u, ks_u, blk_u, row_u,
-                                             idesc1, kd * 9, ch * KSS, b_full, b_empty, rb, abort_flag);
+                ok = issue_taps<T, KSS, RES, false, 3>(p, dcol, tile_cols, ah0, al0, b_desc0, lo_u, ks_u, blk_u, row_u,
+                                                idesc1, kd * 9, ch * KSS, b_full, b_empty, rb, abort_flag);
                 if (ok && kd == 2 && ch == p.nchunks - 1) umma_commit(&acc_full[slot_add(p, s0, d - 2 - un.od0)]);
               }
             }
             umma_commit(&a_empty[ra.idx]);
             ra.next(kAStages);
           }
-          // KDM 3: output plane d - 2 received its last contribution with this plane.
-          if (KDM == 3 && ok && kd_hi == 2) umma_commit(&acc_full[s0 + (uint32_t)(d - 2 - un.od0)]);
+          // KDM 3, 9: output plane d - 2 received its last contribution with this plane.
+          if (KDM != 1 && ok && kd_hi == 2) umma_commit(&acc_full[s0 + (uint32_t)(d - 2 - un.od0)]);
         }
         plane_seq += (uint32_t)(un.od1 - un.od0);
       }
@@ -610,16 +626,22 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
   } else {
     // ------------------------------------------------------------ epilogue
     // Two groups of four warps; each group covers all four TMEM lane quadrants and
-    // takes every other (tile, 16-channel) item of a plane.
+    // takes every other (tile, 16-channel chunk) item of a plane (KDM 9: its half of
+    // the 16 channels, every tile, in one pass).
+    constexpr int CW = 16;
     const int et = tid - kEpiWarp0 * 32;
     const int q = warp & 3;                        // TMEM lane quadrant this warp may access
     const int grp = (warp - kEpiWarp0) >> 2;       // 0 or 1
     const size_t OHW = (size_t)p.OH * p.OW;
     const int PH = p.OH / 2, PW = p.OW / 2;
-    const int cchunks = p.Cout >> 4;
+    const int cchunks = p.Cout / CW;
     const int items = T * cchunks;
     float* s_x = s_epi + grp * (16 * 32);          // pool: h-pair exchange [16][32] per group
     float* s_prev = s_epi + 2 * (16 * 32);         // pool: even-plane maxima [T][Cout][32]
+    // KDM 9: the kw = 1, 2 columns of the first lanes of each quadrant, for the last
+    // lanes of the quadrant before it; [group][2 buffers][T tiles][4 quadrants][24].
+    float* s_kx = s_epi + grp * (2 * T * 4 * 24);
+    uint32_t kx_buf = 0;
     const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
     uint32_t full_par = 0;  // per slot: completions seen so far, mod 2
     uint32_t plane_seq = 0;
@@ -631,19 +653,120 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
       float psum = 0.0f;
       for (int od = un.od0; od < un.od1; ++od) {
         const uint32_t slot = slot_add(p, s0, od - un.od0);
-        if (!(ok = warp_wait(&acc_full[slot], (full_par >> slot) & 1u, p.ctl, abort_flag))) break;
+        // Every epilogue thread takes the same verdict, so that none is left waiting
+        // at a named barrier below for a warp that gave up.
+        ok = named_bar_and(6, kEpiThreads, mbar_wait_bounded(&acc_full[slot], (full_par >> slot) & 1u, p.ctl,
+                                                             abort_flag));
+        if (!ok) break;
         full_par ^= 1u << slot;
         tc_fence_after();
         const bool pool_plane = (EPI == IG3_EPI_POOL_REDUCE) && (od / 2 < p.OD / 2);
+        if constexpr (KDM == 9) {
+          static_assert(EPI != IG3_EPI_POOL_REDUCE, "KDM 9 has no pool-reduce epilogue");
+          // Group g takes channels 8g .. 8g + 7 of every position tile in one pass.
+          // Column block kw holds the sum over kd, kh and channels of the taps with
+          // that kw, at the position of its INPUT pixel: output position o takes
+          // block 0 at o, block 1 at o + 1 and block 2 at o + 2.
+          const int c0 = grp * 8;
+          float v[T][8], a1[T][8], a2[T][8];
+#pragma unroll
+          for (int t = 0; t < T; ++t) {
+            const uint32_t taddr = lane_base + (uint32_t)t * tile_cols + slot * slot_w + (uint32_t)c0;
+            tmem_ld8(taddr, v[t]);
+            tmem_ld8(taddr + (uint32_t)p.Cout, a1[t]);
+            tmem_ld8(taddr + 2u * (uint32_t)p.Cout, a2[t]);
+          }
+          tmem_wait_ld();
+          {
+            float bv[8], zv[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              bv[j] = s_bias[c0 + j];
+              zv[j] = 0.0f;
+            }
+#pragma unroll
+            for (int t = 0; t < T; ++t) {
+              const uint32_t taddr = lane_base + (uint32_t)t * tile_cols + slot * slot_w + (uint32_t)c0;
+              tmem_st8(taddr, bv);  // the slot's next use starts from the bias again
+              tmem_st8(taddr + (uint32_t)p.Cout, zv);
+              tmem_st8(taddr + 2u * (uint32_t)p.Cout, zv);
+            }
+          }
+          float s1[T][8], s2[T][8];
+#pragma unroll
+          for (int t = 0; t < T; ++t)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              s1[t][j] = __shfl_down_sync(0xffffffffu, a1[t][j], 1);
+              s2[t][j] = __shfl_down_sync(0xffffffffu, a2[t][j], 2);
+            }
+          if (p.W > 32) {
+            // A row crosses quadrants: lanes 30 and 31 take the neighbours from the
+            // next quadrant's lanes 0 and 1 (the last quadrant ends a row, where the
+            // two positions are wrap-around columns).  Two buffers alternate, so one
+            // barrier per plane suffices.
+            float* xb = s_kx + kx_buf * (T * 4 * 24);
+            kx_buf ^= 1u;
+            if (q > 0 && lane < 2) {
+#pragma unroll
+              for (int t = 0; t < T; ++t)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  if (lane == 0) {
+                    xb[(t * 4 + q) * 24 + j] = a1[t][j];
+                    xb[(t * 4 + q) * 24 + 8 + j] = a2[t][j];
+                  } else {
+                    xb[(t * 4 + q) * 24 + 16 + j] = a2[t][j];
+                  }
+                }
+            }
+            named_bar_sync(4 + grp, 128);
+            if (q < 3 && lane >= 30) {
+#pragma unroll
+              for (int t = 0; t < T; ++t)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  if (lane == 31) {
+                    s1[t][j] = xb[(t * 4 + q + 1) * 24 + j];
+                    s2[t][j] = xb[(t * 4 + q + 1) * 24 + 16 + j];
+                  } else {
+                    s2[t][j] = xb[(t * 4 + q + 1) * 24 + 8 + j];
+                  }
+                }
+            }
+          }
+#pragma unroll
+          for (int t = 0; t < T; ++t)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[t][j] += s1[t][j] + s2[t][j];
+          // Tiles hold whole rows, so a lane has the same column in every tile.
+          const int lq = q * 32 + lane;
+          const int ow = (p0 + lq) % p.W;
+#pragma unroll
+          for (int t = 0; t < T; ++t) {
+            const int oh = (p0 + t * 128 + lq) / p.W;
+            if (oh < p.OH && ow < p.OW) {
+              float* yb = p.y + (((size_t)un.n * p.Cout + c0) * p.OD + od) * OHW + (size_t)oh * p.OW + ow;
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                float val = v[t][j];
+                if (EPI == IG3_EPI_TANH_MISH) val = tanh_mish(val);
+                yb[(size_t)j * p.OD * OHW] = val;
+              }
+            }
+          }
+        }
+        if constexpr (KDM != 9)
         for (int it = grp; it < items; it += 2) {
           const int t = it / cchunks;
-          const int c0 = (it - t * cchunks) << 4;
+          const int c0 = (it - t * cchunks) * CW;
           const int lp = t * 128 + q * 32 + lane;  // position within the unit
           const int pos = p0 + lp;
           const int oh = pos / p.W, ow = pos - oh * p.W;
           const bool valid = (oh < p.OH) && (ow < p.OW);
           const uint32_t taddr = lane_base + (uint32_t)t * tile_cols + slot * slot_w + (uint32_t)c0;
-          float v[16], bv[16];
+          float v[CW];
+          float bv[16];
           tmem_ld16(taddr, v);
           if constexpr (HL) {
             float v2[16];
@@ -663,7 +786,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
           if constexpr (EPI != IG3_EPI_POOL_REDUCE) {
             float* yb = p.y + (((size_t)un.n * p.Cout + c0) * p.OD + od) * OHW + (size_t)oh * p.OW + ow;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
+            for (int j = 0; j < CW; ++j) {
               float val = v[j];
               if (EPI == IG3_EPI_TANH_MISH) val = tanh_mish(val);
               if (valid) yb[(size_t)j * p.OD * OHW] = val;
@@ -675,24 +798,24 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
             const int cw = ow >> 1;
             const int cell = (r >> 1) * (p.W >> 1) + cw;  // pooled cell within the tile, < 32
             const bool even_w = (ow & 1) == 0, even_r = (r & 1) == 0;
-            float hm[16];
+            float hm[CW];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
+            for (int j = 0; j < CW; ++j) {
               const float z = v[j] * p.inv_div;
               hm[j] = fmaxf(z, __shfl_xor_sync(0xffffffffu, z, 1));
             }
             if (p.W <= 16) {
 #pragma unroll
-              for (int j = 0; j < 16; ++j) hm[j] = fmaxf(hm[j], __shfl_xor_sync(0xffffffffu, hm[j], p.W));
+              for (int j = 0; j < CW; ++j) hm[j] = fmaxf(hm[j], __shfl_xor_sync(0xffffffffu, hm[j], p.W));
             } else {
               if (!even_r && even_w) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) s_x[j * 32 + cell] = hm[j];
+                for (int j = 0; j < CW; ++j) s_x[j * 32 + cell] = hm[j];
               }
               named_bar_sync(1 + grp, 128);
               if (even_r && even_w) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) hm[j] = fmaxf(hm[j], s_x[j * 32 + cell]);
+                for (int j = 0; j < CW; ++j) hm[j] = fmaxf(hm[j], s_x[j * 32 + cell]);
               }
               named_bar_sync(1 + grp, 128);
             }
@@ -700,10 +823,10 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
               float* prev = s_prev + ((size_t)t * p.Cout + c0) * 32 + cell;
               if ((od & 1) == 0) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) prev[j * 32] = hm[j];
+                for (int j = 0; j < CW; ++j) prev[j * 32] = hm[j];
               } else if ((oh >> 1) < PH && cw < PW) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) psum += fmaxf(prev[j * 32], hm[j]);
+                for (int j = 0; j < CW; ++j) psum += fmaxf(prev[j * 32], hm[j]);
               }
             }
           }
@@ -747,6 +870,9 @@ constexpr Variant kVariants[] = {
     {3, 0, 1, 2, 0}, {3, 0, 2, 2, 0}, {3, 0, 1, 1, 1}, {3, 0, 1, 2, 1}, {3, 0, 2, 1, 1}, {3, 0, 2, 2, 1},
     // hi and lo products in separate columns: two MMAs span the window (Cout 16, 32)
     {3, 1, 1, 2, 0}, {3, 1, 2, 2, 0}, {3, 1, 1, 1, 1}, {3, 1, 1, 2, 1}, {3, 1, 2, 1, 1}, {3, 1, 2, 2, 1},
+    // one MMA per split product spans the kd and kw window (Cout 16, W dividing 128;
+    // not pool-reduce)
+    {9, 0, 1, 1, 1}, {9, 0, 1, 2, 1}, {9, 0, 2, 1, 1}, {9, 0, 2, 2, 1}, {9, 0, 1, 2, 0}, {9, 0, 2, 2, 0},
     // one MMA per kd (Cout 96..128)
     {1, 0, 1, 2, 0}, {1, 0, 1, 1, 0},
 };
@@ -777,10 +903,21 @@ int launch_kernel(const TcParams& p, size_t smem, int grid, cudaStream_t stream)
     case 10120: return go(conv3d_tc_kernel<EPI, 1, 1, 2, false, false>);
     case 10110: return go(conv3d_tc_kernel<EPI, 1, 1, 1, false, false>);
     default:
-      return fail(IG3_ERR_UNSUPPORTED,
-                  "conv3d TC: no kernel variant for KDM %d, HL %d, T %d, %d K-steps, resident %d", p.KDM, p.HL, p.T,
-                  p.KSS, p.resident);
+      break;
   }
+  if constexpr (EPI != IG3_EPI_POOL_REDUCE) {
+    switch (key) {
+      case 90111: return go(conv3d_tc_kernel<EPI, 9, 1, 1, true, false>);
+      case 90121: return go(conv3d_tc_kernel<EPI, 9, 1, 2, true, false>);
+      case 90211: return go(conv3d_tc_kernel<EPI, 9, 2, 1, true, false>);
+      case 90221: return go(conv3d_tc_kernel<EPI, 9, 2, 2, true, false>);
+      case 90120: return go(conv3d_tc_kernel<EPI, 9, 1, 2, false, false>);
+      case 90220: return go(conv3d_tc_kernel<EPI, 9, 2, 2, false, false>);
+      default: break;
+    }
+  }
+  return fail(IG3_ERR_UNSUPPORTED, "conv3d TC: no kernel variant for KDM %d, HL %d, T %d, %d K-steps, resident %d",
+              p.KDM, p.HL, p.T, p.KSS, p.resident);
 }
 
 extern template int launch_kernel<IG3_EPI_NONE>(const TcParams&, size_t, int, cudaStream_t);

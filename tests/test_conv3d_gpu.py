@@ -63,6 +63,13 @@ SMALL_CASES = [
     (1, 12, 5, 8, 20, 96),    # Cout = 96: one MMA per kd over a ring of five slots
     (1, 8, 6, 9, 16, 112),    # Cout = 112: one MMA per kd, four slots
     (2, 72, 4, 6, 24, 64),    # Cin = 72: several channel chunks of streamed weights
+    (1, 8, 5, 6, 4, 16),      # Cout = 16, kw inside the MMA (window over kd and kw): W = 4
+    (2, 8, 6, 12, 32, 16),    #   W = 32: rows end at quadrant ends
+    (1, 8, 6, 12, 128, 16),   #   W = 128: one row per tile, three quadrant crossings
+    (2, 8, 10, 64, 64, 16),   #   two position tiles per unit
+    (1, 40, 5, 6, 64, 16),    #   five K-steps of resident weights
+    (1, 136, 5, 6, 64, 16),   #   streamed weights
+    (1, 8, 5, 9, 20, 16),     # Cout = 16 with W not dividing 128: hi and lo columns instead
     (2, 3, 5, 7, 9, 5),       # odd channel counts
     (1, 1, 3, 3, 3, 1),       # smallest valid input: one output
 ]
@@ -144,6 +151,10 @@ POOL_CASES = [
     (2, 4, 7, 9, 13, 16),     # odd conv-output dims: floor mode drops a plane, row, column
     (1, 5, 4, 4, 4, 3),       # smallest pooled grid (1x1x1), odd channels
     (2, 16, 5, 12, 32, 32),   # W = 32, odd conv-output depth
+    (2, 8, 6, 10, 16, 16),    # W = 16: h-pair by lane shuffle
+    (2, 8, 6, 10, 32, 16),    # W = 32
+    (1, 8, 6, 12, 4, 16),     # W = 4
+    (2, 8, 8, 64, 64, 16),    # two position tiles per unit
 ]
 
 
