@@ -165,7 +165,9 @@ int positions_tiles(int OH, int W, int T) { return ((OH * W) + T * 128 - 1) / (T
 // max(70, N/2 + 5) cycles (one thread issues them; N/2 is the M = 128, K = 8 execution
 // time) and every streamed weight stage ~250 more.  The chunk's input convert runs
 // alongside: ~0.9 cycles per value when the convert warps load x themselves (latency
-// bound), ~0.35 when a bulk-copy loader stages it ahead.
+// bound), ~0.35 when a bulk-copy loader stages it ahead.  Each A chunk also costs
+// the issuing thread ~900 cycles of hand-over (mbarrier tests, which queue behind the
+// MMAs' shared-memory operand reads, and commits), not hidden by the shallow MMA queue.
 //
 // KDM 9: three MMAs (one per split product) per (kh, K-step, tile) with N = 3 * nkd *
 // Cout.  At this N an MMA is bound as much by shared-memory reads (A 4 KB + B 32 B
@@ -178,7 +180,7 @@ double plane_cycles(int kdm, int hl, int nkd, int Cout, int KS, int nchunks, int
     const double exec = mmas * (0.5 * n + 5.0) + (res ? 0.0 : 250.0 * 3.0 * nchunks);
     const double port = (mmas * (4096.0 + 32.0 * n) + npos * 8.0 * KS * 16.0) / 128.0;
     const double conv = (xstage ? 0.35 : 0.9) * npos * (8.0 * KS);
-    return 1.1 * std::max(std::max(exec, port), conv) + 300.0 * nchunks;
+    return 1.1 * std::max(std::max(exec, port), conv) + 900.0 * nchunks;
   }
   const int mmas_per_step = (kdm == 3) ? (hl ? 2 : 3) : 3 * nkd;
   const int n = (kdm == 3) ? nkd * Cout * (hl ? 2 : 1) : Cout;
@@ -186,7 +188,7 @@ double plane_cycles(int kdm, int hl, int nkd, int Cout, int KS, int nchunks, int
   const double stages = res ? 0.0 : 9.0 * nchunks * (kdm == 3 ? 1 : nkd);
   const double mma = mmas * std::max(70.0, 0.5 * n + 5.0) + 250.0 * stages;
   const double conv = (xstage ? 0.35 : 0.9) * npos * (8.0 * KS);
-  return std::max(mma, conv) + 300.0 * nchunks;  // A hand-over per chunk
+  return std::max(mma, conv) + 900.0 * nchunks;  // A hand-over per chunk (mbarrier tests, commits)
 }
 
 double unit_cycles(int kdm, int hl, int planes, int Cout, int KS, int nchunks, int T, bool res, int npos,

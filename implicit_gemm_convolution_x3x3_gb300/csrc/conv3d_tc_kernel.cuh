@@ -116,11 +116,46 @@ static __device__ __forceinline__ bool mbar_test_wait(uint32_t bar_addr, uint32_
   return done != 0;
 }
 
+// The bounded wait of the MMA-issuing thread for its per-chunk hand-offs with resident
+// weights, entirely inline: with MMAs in flight, a function call in the issue loop
+// (even one never taken) slows every tcgen05.mma issue (measured: ~135 cycles more per
+// wait than this form at N = 128; pool-reduce 0.547 -> 0.506 ms).  With streamed
+// weights the loop also holds the per-tap weight-stage waits, and there the inline
+// form measured 1-2% slower (and 13% slower as the per-tap wait): those keep
+// wait_fast.
+// Same contract as mbar_wait_bounded: the abort flag is polled, and past the time
+// limit the wait sets it, records the timeout and returns false.
+static __device__ __forceinline__ bool wait_issue(uint64_t* bar, uint32_t parity, const WaitCtl& ctl,
+                                                  volatile int* abort) {
+  const uint32_t a = smem_addr(bar);
+  if (mbar_test_wait(a, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_test_wait(a, parity)) return true;
+    if ((i & 255u) == 0u) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > ctl.limit_ns) {
+        *abort = 1;
+        atomicOr(ctl.status, kDevStatusTimeout);
+        return false;
+      }
+    }
+  }
+}
+
 // The common case inline (phase already complete), the bounded loop out of line.
 static __device__ __forceinline__ bool wait_fast(uint64_t* bar, uint32_t parity, const WaitCtl& ctl,
                                                  volatile int* abort) {
   if (mbar_test_wait(smem_addr(bar), parity)) return true;
   return mbar_wait_bounded(bar, parity, ctl, abort);
+}
+
+// The MMA issuer's per-chunk wait: inline with resident weights, wait_fast otherwise.
+template <bool INLINE>
+static __device__ __forceinline__ bool wait_mma(uint64_t* bar, uint32_t parity, const WaitCtl& ctl,
+                                                volatile int* abort) {
+  if constexpr (INLINE) return wait_issue(bar, parity, ctl, abort);
+  else return wait_fast(bar, parity, ctl, abort);
 }
 
 // The MMAs of one weight stage (KSS K-steps x T position tiles), fully unrolled so
@@ -388,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
       const uint32_t cout = (uint32_t)p.Cout;
       const uint32_t idesc1 = umma_idesc_tf32(128, p.Cout);
       bool ok = true;
-      if constexpr (RES) ok = mbar_wait_bounded(w_full, 0, p.ctl, abort_flag);
+      if constexpr (RES) ok = wait_issue(w_full, 0, p.ctl, abort_flag);
       Ring ra, rb;
       uint32_t empty_par = 0;  // per slot: uses so far, mod 2
       uint32_t plane_seq = 0;
@@ -399,12 +434,12 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
           // Output planes fed by input plane d: od = d - kd for kd in [kd_lo, kd_hi].
           const int kd_hi = min(2, d - un.od0), kd_lo = max(0, d - un.od1 + 1);
           for (int ch = 0; ok && ch < p.nchunks; ++ch) {
-            if (!(ok = wait_fast(&a_full[ra.idx], ra.phase, p.ctl, abort_flag))) break;
+            if (!(ok = wait_mma<RES>(&a_full[ra.idx], ra.phase, p.ctl, abort_flag))) break;
             tc_fence_after();
             if (ch == 0 && kd_lo == 0) {
               // Plane d opens output plane od = d: its slot must have been drained.
               const uint32_t s = slot_add(p, s0, d - un.od0);
-              if (!(ok = wait_fast(&acc_empty[s], ((empty_par >> s) & 1u) ^ 1u, p.ctl, abort_flag))) break;
+              if (!(ok = wait_mma<RES>(&acc_empty[s], ((empty_par >> s) & 1u) ^ 1u, p.ctl, abort_flag))) break;
               empty_par ^= 1u << s;
               tc_fence_after();
             }
