@@ -209,6 +209,7 @@ static __device__ __forceinline__ bool issue_taps(const TcParams& p, uint32_t dc
   const uint32_t b_stage_u = blk_u * (uint32_t)KSS;
 #pragma unroll
   for (int kh = 0; kh < 3; ++kh) {
+    bool row_ready = false;
 #pragma unroll
     for (int kw = 0; kw < NKW; ++kw) {
       const uint64_t tap_u = (uint64_t)((uint32_t)kh * row_u + (uint32_t)kw);
@@ -216,7 +217,20 @@ static __device__ __forceinline__ bool issue_taps(const TcParams& p, uint32_t dc
       if constexpr (RES) {
         bst = bwin + (uint64_t)((uint32_t)((tap_base + kh * NKW + kw) * p.KS + blk0) * blk_u);
       } else {
-        if (!wait_fast(&b_full[rb.idx], rb.phase, p.ctl, abort_flag)) good = false;
+        if (NKW == 3 && kw == 0) {
+          // Test the row's three stages together: with MMAs in flight each test waits
+          // behind their operand reads, and three back-to-back tests cost about one.
+          // (A stage not yet refilled reads as not ready.)
+          uint32_t i1 = rb.idx + 1, ph1 = rb.phase;
+          if (i1 == (uint32_t)p.SB) { i1 = 0; ph1 ^= 1u; }
+          uint32_t i2 = i1 + 1, ph2 = ph1;
+          if (i2 == (uint32_t)p.SB) { i2 = 0; ph2 ^= 1u; }
+          const bool r0 = mbar_test_wait(smem_addr(&b_full[rb.idx]), rb.phase);
+          const bool r1 = mbar_test_wait(smem_addr(&b_full[i1]), ph1);
+          const bool r2 = mbar_test_wait(smem_addr(&b_full[i2]), ph2);
+          row_ready = r0 && r1 && r2;
+        }
+        if (!row_ready && !wait_fast(&b_full[rb.idx], rb.phase, p.ctl, abort_flag)) good = false;
         tc_fence_after();
         bst = bwin + (uint64_t)(rb.idx * b_stage_u);
       }
