@@ -12,6 +12,9 @@ numpy-facing functions.  Every function returns float64.
 Parity status of each function (what pins it; see tests/test_oracle_pins.py):
   conv3d / conv3d_at       pinned: brute-force im2col x W^T, scipy correlate,
                            delta kernel, constant input, linearity, translation.
+  conv3d_pad / _at         pinned: np.pad + brute-force im2col, scipy correlate in
+                           'same' mode, delta kernel (y = x), constant-input corner and
+                           interior closed forms, pad 0 == conv3d.
   tanh_mish                pinned: algebraic identity form, special values,
                            large-y asymptote, Mish minimum.
   pool_reduce              pinned: window enumeration, S/(div*cells)+sum(bias2)
@@ -65,6 +68,11 @@ def _load():
                                          _i64, _i64, _i64, _i64, _i64]
         lib.oracle_conv3d.restype = None
         lib.oracle_conv3d.argtypes = [_fp, _i64, _i64, _i64, _i64, _i64, _fp, _i64, _fp, _dp]
+        lib.oracle_conv3d_pad_at.restype = ctypes.c_double
+        lib.oracle_conv3d_pad_at.argtypes = [_fp, _i64, _i64, _i64, _i64, _i64, _i64, _fp, _i64, _fp,
+                                             _i64, _i64, _i64, _i64, _i64]
+        lib.oracle_conv3d_pad.restype = None
+        lib.oracle_conv3d_pad.argtypes = [_fp, _i64, _i64, _i64, _i64, _i64, _i64, _fp, _i64, _fp, _dp]
         lib.oracle_tanh_mish.restype = ctypes.c_double
         lib.oracle_tanh_mish.argtypes = [ctypes.c_double]
         lib.oracle_tanh_mish_array.restype = None
@@ -152,6 +160,35 @@ def conv3d_at(x, w, b, index) -> np.ndarray:
     for i, (n, k, od, oh, ow) in enumerate(idx):
         out[i] = lib.oracle_conv3d_at(xp, N, Cin, D, H, W, wp, Cout, bp,
                                       int(n), int(k), int(od), int(oh), int(ow))
+    return out
+
+
+def conv3d_pad(x, w, b=None, pad: int = 1) -> np.ndarray:
+    """Zero-padded stride-1 3x3x3 cross-correlation, float64 [N,Cout,D+2P-2,H+2P-2,W+2P-2]."""
+    lib = _load()
+    x = _f32(x); w = _f32(w); b = None if b is None else _f32(b)
+    N, Cin, D, H, W = x.shape
+    Cout = w.shape[0]
+    assert w.shape == (Cout, Cin, 3, 3, 3) and pad >= 0
+    OD, OH, OW = D + 2 * pad - 2, H + 2 * pad - 2, W + 2 * pad - 2
+    y = np.empty((N, Cout, max(OD, 0), max(OH, 0), max(OW, 0)), dtype=np.float64)
+    lib.oracle_conv3d_pad(_fptr(x), N, Cin, D, H, W, int(pad), _fptr(w), Cout, _fptr(b),
+                          y.ctypes.data_as(_dp))
+    return y
+
+
+def conv3d_pad_at(x, w, b, pad: int, index) -> np.ndarray:
+    """Padded conv outputs at a list of (n, k, od, oh, ow) indices (float64)."""
+    lib = _load()
+    x = _f32(x); w = _f32(w); b = None if b is None else _f32(b)
+    N, Cin, D, H, W = x.shape
+    Cout = w.shape[0]
+    idx = np.asarray(index, dtype=np.int64).reshape(-1, 5)
+    out = np.empty(len(idx), dtype=np.float64)
+    xp, wp, bp = _fptr(x), _fptr(w), _fptr(b)
+    for i, (n, k, od, oh, ow) in enumerate(idx):
+        out[i] = lib.oracle_conv3d_pad_at(xp, N, Cin, D, H, W, int(pad), wp, Cout, bp,
+                                          int(n), int(k), int(od), int(oh), int(ow))
     return out
 
 

@@ -86,6 +86,47 @@ void oracle_conv3d(const float* x, i64 N, i64 Cin, i64 D, i64 H, i64 W,
 }
 
 /*
+ * One output of the zero-padded, stride-1, 3x3x3 cross-correlation with padding P:
+ *   y[n,k,od,oh,ow] = b[k] + sum_{c,kd,kh,kw} w[k,c,kd,kh,kw] * x[n,c,od+kd-P,oh+kh-P,ow+kw-P]
+ * where x reads as zero outside [0,D) x [0,H) x [0,W); output size D+2P-2 etc.
+ * [P47] the padding discussion: the input coordinate of an output is shifted by
+ * -padding, the bounds check covers both ends and loads zero outside, and the output
+ * size is (D + 2*padding - KD)/stride + 1.
+ */
+double oracle_conv3d_pad_at(const float* x, i64 N, i64 Cin, i64 D, i64 H, i64 W, i64 P,
+                            const float* w, i64 Cout, const float* b,
+                            i64 n, i64 k, i64 od, i64 oh, i64 ow) {
+  (void)N; (void)Cout;
+  double acc = (b != NULL) ? (double)b[k] : 0.0;
+  for (i64 c = 0; c < Cin; ++c)
+    for (i64 kd = 0; kd < 3; ++kd)
+      for (i64 kh = 0; kh < 3; ++kh)
+        for (i64 kw = 0; kw < 3; ++kw) {
+          const i64 d = od + kd - P, h = oh + kh - P, ww = ow + kw - P;
+          if (d < 0 || d >= D || h < 0 || h >= H || ww < 0 || ww >= W) continue;  /* zero */
+          double xv = (double)x[(((n * Cin + c) * D + d) * H + h) * W + ww];
+          double wv = (double)w[(((k * Cin + c) * 3 + kd) * 3 + kh) * 3 + kw];
+          acc += wv * xv;
+        }
+  return acc;
+}
+
+/* The whole padded conv output, y[N][Cout][D+2P-2][H+2P-2][W+2P-2] in float64. */
+void oracle_conv3d_pad(const float* x, i64 N, i64 Cin, i64 D, i64 H, i64 W, i64 P,
+                       const float* w, i64 Cout, const float* b, double* y) {
+  const i64 OD = D + 2 * P - 2, OH = H + 2 * P - 2, OW = W + 2 * P - 2;
+  if (OD <= 0 || OH <= 0 || OW <= 0) return;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+  for (i64 n = 0; n < N; ++n)
+    for (i64 k = 0; k < Cout; ++k)
+      for (i64 od = 0; od < OD; ++od)
+        for (i64 oh = 0; oh < OH; ++oh)
+          for (i64 ow = 0; ow < OW; ++ow)
+            y[(((n * Cout + k) * OD + od) * OH + oh) * OW + ow] =
+                oracle_conv3d_pad_at(x, N, Cin, D, H, W, P, w, Cout, b, n, k, od, oh, ow);
+}
+
+/*
  * out = tanh(mish(y)), mish(y) = y * tanh(softplus(y)), softplus(y) = log(1 + e^y).
  * [P47] the activation description ("PyTorch computes mish first, then tanh").
  * Softplus is evaluated as log1p(exp(y)) with no threshold: for large y, exp

@@ -171,6 +171,72 @@ def test_conv3d_at_matches_full():
     assert np.array_equal(oracle.conv3d_at(t["x"], t["w"], t["b"], idx), y[tuple(idx.T)])
 
 
+# ------------------------------------------------------------------ padded conv3d
+# [P47] the padding discussion: input coordinate od + kd - padding, zero outside the
+# tensor, output size D + 2*padding - 2.
+@pytest.mark.parametrize("shape,pad", [((1, 2, 3, 4, 5, 3), 1), ((2, 3, 4, 3, 6, 2), 1),
+                                       ((1, 2, 3, 3, 3, 2), 2), ((1, 1, 1, 1, 1, 1), 1),
+                                       ((2, 2, 5, 4, 3, 2), 0)])
+def test_conv3d_pad_vs_numpy_pad_and_im2col(shape, pad):
+    N, Cin, D, H, W, Cout = shape
+    rng = np.random.default_rng(100 + sum(shape) + pad)
+    x = rng.standard_normal((N, Cin, D, H, W)).astype(np.float32)
+    w = rng.uniform(-1, 1, (Cout, Cin, 3, 3, 3)).astype(np.float32)
+    b = rng.uniform(-1, 1, Cout).astype(np.float32)
+    xp = np.pad(x, ((0, 0), (0, 0), (pad, pad), (pad, pad), (pad, pad)))
+    y = oracle.conv3d_pad(x, w, b, pad)
+    assert y.shape == (N, Cout, D + 2 * pad - 2, H + 2 * pad - 2, W + 2 * pad - 2)
+    assert rel_err(y, im2col_conv3d(xp, w, b)) < 1e-12
+
+
+def test_conv3d_pad_vs_scipy_same():
+    rng = np.random.default_rng(101)
+    x = rng.standard_normal((1, 2, 5, 6, 4)).astype(np.float32)
+    w = rng.uniform(-1, 1, (3, 2, 3, 3, 3)).astype(np.float32)
+    ref = np.zeros((1, 3, 5, 6, 4))
+    for k in range(3):
+        for c in range(2):
+            ref[0, k] += scipy.signal.correlate(x[0, c].astype(np.float64), w[k, c].astype(np.float64),
+                                                mode="same", method="direct")
+    assert rel_err(oracle.conv3d_pad(x, w, None, 1), ref) < 1e-12
+
+
+def test_conv3d_pad_delta_kernel_is_identity():
+    rng = np.random.default_rng(102)
+    C = 3
+    x = rng.standard_normal((2, C, 4, 5, 6)).astype(np.float32)
+    w = np.zeros((C, C, 3, 3, 3), np.float32)
+    for k in range(C):
+        w[k, k, 1, 1, 1] = 1.0
+    assert np.array_equal(oracle.conv3d_pad(x, w, None, 1), x.astype(np.float64))
+
+
+def test_conv3d_pad_constant_input_corner_and_interior():
+    rng = np.random.default_rng(103)
+    x = np.ones((1, 2, 5, 5, 5), np.float32)
+    w = rng.uniform(-1, 1, (3, 2, 3, 3, 3)).astype(np.float32)
+    b = rng.uniform(-1, 1, 3).astype(np.float32)
+    y = oracle.conv3d_pad(x, w, b, 1)
+    w64 = w.astype(np.float64)
+    # Corner (0,0,0): only taps with kd, kh, kw >= 1 land inside.
+    corner = b + w64[:, :, 1:, 1:, 1:].reshape(3, -1).sum(1)
+    # Interior: every tap lands inside.
+    interior = b + w64.reshape(3, -1).sum(1)
+    assert rel_err(y[0, :, 0, 0, 0], corner) < 1e-13
+    assert rel_err(y[0, :, 2, 2, 2], interior) < 1e-13
+
+
+def test_conv3d_pad_zero_equals_valid_and_at_matches_full():
+    rng = np.random.default_rng(104)
+    x = rng.standard_normal((1, 2, 5, 6, 7)).astype(np.float32)
+    w = rng.uniform(-1, 1, (2, 2, 3, 3, 3)).astype(np.float32)
+    b = rng.uniform(-1, 1, 2).astype(np.float32)
+    assert np.array_equal(oracle.conv3d_pad(x, w, b, 0), oracle.conv3d(x, w, b))
+    y = oracle.conv3d_pad(x, w, b, 1)
+    idx = np.stack([rng.integers(0, s, 40) for s in y.shape], 1)
+    assert np.array_equal(oracle.conv3d_pad_at(x, w, b, 1, idx), y[tuple(idx.T)])
+
+
 # ------------------------------------------------------------------ tanh(mish)
 def test_tanh_mish_zero():
     assert oracle.tanh_mish_scalar(0.0) == 0.0
