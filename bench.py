@@ -54,6 +54,7 @@ WORKLOADS = {
     "sweep64": lambda: si.conv3d_sweep(64),
     "sweep128": lambda: si.conv3d_sweep(128),
     "tiny": si.tiny_conv3d,
+    "conv3d_same": si.conv3d_same_tanh_mish,
 }
 
 
@@ -66,10 +67,16 @@ def with_batch(wl, n: int):
 
 
 # ------------------------------------------------------------------ workload arithmetic
+def conv_out_dims(wl) -> tuple:
+    d, p = wl.dims, wl.pad
+    return d["D"] + 2 * p - 2, d["H"] + 2 * p - 2, d["W"] + 2 * p - 2
+
+
 def macs(wl) -> int:
     d = wl.dims
     if wl.op == "conv3d":
-        return d["N"] * d["Cout"] * (d["D"] - 2) * (d["H"] - 2) * (d["W"] - 2) * d["Cin"] * 27
+        od, oh, ow = conv_out_dims(wl)
+        return d["N"] * d["Cout"] * od * oh * ow * d["Cin"] * 27
     return d["N"] * d["H"] * d["W"] * d["C"] * (9 + d["Cout"])
 
 
@@ -81,7 +88,8 @@ def compulsory_bytes(wl) -> tuple:
         if wl.epilogue == "pool_reduce":
             wr = d["N"] * 4
         else:
-            wr = d["N"] * d["Cout"] * (d["D"] - 2) * (d["H"] - 2) * (d["W"] - 2) * 4
+            od, oh, ow = conv_out_dims(wl)
+            wr = d["N"] * d["Cout"] * od * oh * ow * 4
     else:
         wr = d["N"] * d["Cout"] * d["H"] * d["W"] * 4
     return rd, wr
@@ -92,7 +100,8 @@ def describe(wl) -> str:
     if wl.op == "conv3d":
         epi = {"tanh_mish": "tanh(mish)", "pool_reduce": "/2-maxpool2-mean-+bias2-sum_c",
                "none": "none"}[wl.epilogue]
-        return (f"conv3d k3 valid s1 x[{d['N']},{d['Cin']},{d['D']},{d['H']},{d['W']}] "
+        kind = f"pad{wl.pad}" if wl.pad else "valid"
+        return (f"conv3d k3 {kind} s1 x[{d['N']},{d['Cin']},{d['D']},{d['H']},{d['W']}] "
                 f"w[{d['Cout']},{d['Cin']},3,3,3] epilogue {epi}")
     return (f"dwsep conv2d x[{d['N']},{d['C']},{d['H']},{d['W']}] dw 3x3 pad1 -> pw "
             f"{d['C']}->{d['Cout']}, no bias")
@@ -226,16 +235,17 @@ def make_call(ig3, wl, dev_t: dict, path: str):
             params = {"divisor": wl.divisor, "pool": wl.pool, "bias2": dev_t["bias2"]}
             out = torch.empty((d["N"],), device=dev_t["x"].device)
         else:
-            out = torch.empty((d["N"], d["Cout"], d["D"] - 2, d["H"] - 2, d["W"] - 2), device=dev_t["x"].device)
-        need = ig3.conv3d_fused_workspace_size(d["N"], d["Cin"], d["D"], d["H"], d["W"], d["Cout"],
-                                               wl.epilogue, path)
+            out = torch.empty((d["N"], d["Cout"]) + conv_out_dims(wl), device=dev_t["x"].device)
+        p2 = 2 * wl.pad
+        need = ig3.conv3d_fused_pad_workspace_size(d["N"], d["Cin"], d["D"], d["H"], d["W"], wl.pad, d["Cout"],
+                                                   wl.epilogue, path)
         ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev_t["x"].device)
-        chosen = ig3.conv3d_fused_select_path(d["N"], d["Cin"], d["D"], d["H"], d["W"], d["Cout"], wl.epilogue,
-                                              path)
+        chosen = ig3.conv3d_fused_select_path(d["N"], d["Cin"], d["D"] + p2, d["H"] + p2, d["W"] + p2, d["Cout"],
+                                              wl.epilogue, path)
 
         def call():
             ig3.conv3d_fused(dev_t["x"], dev_t["w"], dev_t.get("b"), epilogue=wl.epilogue, params=params, out=out,
-                             workspace=ws, path=path)
+                             workspace=ws, path=path, pad=wl.pad)
         return call, out, chosen
     d = wl.dims
     out = torch.empty((d["N"], d["Cout"], d["H"], d["W"]), device=dev_t["x"].device)
@@ -378,23 +388,26 @@ def oracle_sample(wl, target_s: float):
     t = shard_inputs(wl, 0, 1)
     d = wl.dims
     if wl.op == "conv3d":
+        _, oh, ow = conv_out_dims(wl)
+
         def make(planes):
-            xs = np.ascontiguousarray(t["x"][0:1, :, 0:planes + 2])
+            xs = np.ascontiguousarray(t["x"][0:1, :, 0:planes + 2 - 2 * wl.pad])
 
             def run():
                 t0 = time.perf_counter()
-                y = oracle.conv3d(xs, t["w"], t.get("b"))
+                y = oracle.conv3d_pad(xs, t["w"], t.get("b"), wl.pad)
                 if wl.epilogue == "tanh_mish":
                     oracle.tanh_mish(y)
                 elif wl.epilogue == "pool_reduce":
                     oracle.pool_reduce(y, wl.divisor, wl.pool, t["bias2"])
                 return time.perf_counter() - t0
-            return run, 2.0 * d["Cout"] * planes * (d["H"] - 2) * (d["W"] - 2) * d["Cin"] * 27
+            return run, 2.0 * d["Cout"] * planes * oh * ow * d["Cin"] * 27
         one, _ = make(2)
         dt = one()
-        planes = int(max(2, min(d["D"] - 2, 2 * target_s / max(dt, 1e-3))))
+        od = conv_out_dims(wl)[0]
+        planes = int(max(2, min(od, 2 * target_s / max(dt, 1e-3))))
         run, fl = make(planes)
-        return run, fl, f"batch item 0, {planes} of {d['D'] - 2} output planes, all {d['Cout']} channels"
+        return run, fl, f"batch item 0, {planes} of {od} output planes, all {d['Cout']} channels"
 
     def make(rows):
         xs = np.ascontiguousarray(t["x"][0:1, :, 0:rows])
@@ -448,7 +461,7 @@ def run_ours(args) -> None:
 
     others = []
     if rank == 0 and not args.no_others and world == 1:
-        for name in ["tiny", "conv3d_pool_reduce", "dwsep", "sweep16", "sweep64", "sweep128"]:
+        for name in ["tiny", "conv3d_pool_reduce", "dwsep", "sweep16", "sweep64", "sweep128", "conv3d_same"]:
             if name == args.workload:
                 continue
             owl = WORKLOADS[name]()

@@ -160,6 +160,14 @@ int num_sms() {
   return d ? d->sms : 0;
 }
 
+int conv3d_select_quiet(int N, int Cin, int D, int H, int W, int Cout, int epi, int path) {
+  char saved[sizeof(t_last_error)];
+  snprintf(saved, sizeof(saved), "%s", t_last_error);
+  const int p = conv3d_select(N, Cin, D, H, W, Cout, epi, path);
+  snprintf(t_last_error, sizeof(t_last_error), "%s", saved);
+  return p;
+}
+
 int selftest_bounded_wait(unsigned long long timeout_ns, cudaStream_t stream) {
   DeviceInfo* d = current_device();
   if (!d) return fail(IG3_ERR_CUDA, "ig3_selftest_bounded_wait: device set-up failed");
@@ -175,10 +183,7 @@ using namespace ig3;
 extern "C" {
 
 size_t conv3d_fused_workspace_size(int N, int Cin, int D, int H, int W, int Cout, int epilogue, int path) {
-  char saved[sizeof(t_last_error)];
-  snprintf(saved, sizeof(saved), "%s", t_last_error);
-  const int p = conv3d_select(N, Cin, D, H, W, Cout, epilogue, path);
-  snprintf(t_last_error, sizeof(t_last_error), "%s", saved);
+  const int p = ig3::conv3d_select_quiet(N, Cin, D, H, W, Cout, epilogue, path);
   if (p < 0) return 0;
   Conv3dArgs a{};
   a.N = N; a.Cin = Cin; a.D = D; a.H = H; a.W = W; a.Cout = Cout; a.epi = epilogue;

@@ -55,6 +55,9 @@ int num_sms();
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// conv3d_fused_select_path without touching ig3_last_error() (for size queries).
+int conv3d_select_quiet(int N, int Cin, int D, int H, int W, int Cout, int epi, int path);
+
 // ---- FMA path (conv3d_fma.cu)
 size_t conv3d_fma_workspace(const Conv3dArgs& a);
 int conv3d_fma_launch(const Conv3dArgs& a);

@@ -102,6 +102,30 @@ int conv3d_fused(const float* x, int N, int Cin, int D, int H, int W,
                  float* y, void* workspace, size_t workspace_bytes,
                  int path, void* stream);
 
+/*
+ * Zero-padded stride-1 3x3x3 cross-correlation with a fused epilogue ([P47], the
+ * padding discussion: the input coordinate of an output is shifted by -pad, reads
+ * outside the tensor give zero, the output size is D + 2*pad - 2):
+ *   conv[n,k,od,oh,ow] = b[k] + sum_{c,kd,kh,kw} w[k,c,kd,kh,kw] * x[n,c,od+kd-pad,oh+kh-pad,ow+kw-pad]
+ * for od < D+2*pad-2, oh < H+2*pad-2, ow < W+2*pad-2 (pad = 1 keeps D, H, W).
+ *
+ * Arguments are those of conv3d_fused plus pad (0..16; 0 is conv3d_fused itself),
+ * with every output size read as D+2*pad-2 etc. (POOL_REDUCE pools that grid).  The
+ * library writes the zero-bordered copy [N][Cin][D+2*pad][H+2*pad][W+2*pad] of x at
+ * the start of the workspace and runs conv3d_fused on it, so the workspace holds that
+ * copy too: conv3d_fused_pad_workspace_size bytes (never 0 when pad > 0), 256-byte
+ * aligned.  The path (and its requirements) is the one conv3d_fused takes for the
+ * padded dimensions.  Requires D, H, W >= 1 and the padded copy below 2^31 elements;
+ * there is no no-allocation variant.
+ */
+size_t conv3d_fused_pad_workspace_size(int N, int Cin, int D, int H, int W, int pad, int Cout,
+                                       int epilogue, int path);
+int conv3d_fused_pad(const float* x, int N, int Cin, int D, int H, int W, int pad,
+                     const float* w, int Cout, const float* b,
+                     int epilogue, const ig3_epi_params* params,
+                     float* y, void* workspace, size_t workspace_bytes,
+                     int path, void* stream);
+
 /* Size of the library's own scratch buffer used by conv3d_fused_noalloc (4 MiB). */
 #define IG3_NOALLOC_SCRATCH_BYTES (4u * 1024u * 1024u)
 

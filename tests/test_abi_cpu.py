@@ -139,3 +139,40 @@ def test_workspace_query_is_zero_for_rejected_args(lib):
     lib.conv3d_fused_workspace_size.restype = ctypes.c_size_t
     assert lib.conv3d_fused_workspace_size(0, 1, 3, 3, 3, 1, 1, 0) == 0
     assert lib.conv3d_fused_workspace_size(1, 1, 3, 3, 3, 1, 1, 2) == 0  # tanh-mish on FMA needs none
+
+
+def _pad(lib):
+    f = lib.conv3d_fused_pad
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] + [ctypes.c_int] * 6 + [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                                                           ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                                           ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int,
+                                                           ctypes.c_void_p]
+    return f
+
+
+def test_conv3d_pad_argument_errors(lib):
+    f = _pad(lib)
+    q = lib.conv3d_fused_pad_workspace_size
+    q.restype = ctypes.c_size_t
+    # pad out of range, non-positive dims, too many padded elements: rejected before any launch
+    assert f(FAKE, 1, 1, 3, 3, 3, -1, FAKE, 1, None, 1, None, FAKE, FAKE, 1 << 20, 2, None) == -1
+    assert f(FAKE, 1, 1, 3, 3, 3, 17, FAKE, 1, None, 1, None, FAKE, FAKE, 1 << 20, 2, None) == -1
+    assert f(FAKE, 1, 1, 0, 3, 3, 1, FAKE, 1, None, 1, None, FAKE, FAKE, 1 << 20, 2, None) == -1
+    assert f(FAKE, 2048, 64, 62, 62, 62, 1, FAKE, 1, None, 1, None, FAKE, FAKE, 1 << 20, 2, None) == -1
+    # the TC path's own requirements apply to the padded shape (Cout = 2)
+    assert f(FAKE, 1, 1, 3, 3, 3, 1, FAKE, 2, None, 1, None, FAKE, FAKE, 1 << 20, 1, None) == -2
+    # a single voxel with pad 1 is a valid 1x1x1 output; it needs the bordered copy
+    need = q(1, 1, 1, 1, 1, 1, 1, 1, 2)
+    assert need >= 27 * 4 and need % 256 == 0
+    assert f(FAKE, 1, 1, 1, 1, 1, 1, FAKE, 1, None, 1, None, FAKE, None, 0, 2, None) == -5
+    assert f(FAKE, 1, 1, 1, 1, 1, 1, FAKE, 1, None, 1, None, FAKE, FAKE, need - 1, 2, None) == -5
+    assert f(FAKE, 1, 1, 1, 1, 1, 1, FAKE, 1, None, 1, None, FAKE, FAKE + 4, need, 2, None) == -5
+    # queries: zero for rejected arguments; pad 0 is the valid-conv query
+    assert q(1, 1, 3, 3, 3, -1, 1, 1, 2) == 0
+    assert q(0, 1, 3, 3, 3, 1, 1, 1, 2) == 0
+    lib.conv3d_fused_workspace_size.restype = ctypes.c_size_t
+    assert q(1, 1, 4, 4, 4, 0, 1, 2, 2) == lib.conv3d_fused_workspace_size(1, 1, 4, 4, 4, 1, 2, 2)
+    # pad 1: the bordered copy [1][2][6][7][8] (256-byte aligned) plus the valid query of that shape
+    assert q(1, 2, 4, 5, 6, 1, 16, 1, 1) == \
+        (2 * 6 * 7 * 8 * 4 + 255) // 256 * 256 + lib.conv3d_fused_workspace_size(1, 2, 6, 7, 8, 16, 1, 1)

@@ -241,3 +241,76 @@ def test_conv3d_misaligned_input(ig3, shape, epi):
         out = ig3.conv3d_fused(x, w, b, epilogue=epi, params=dev_params, path=path)
         assert ig3.ig3_last_device_status() == 0
         assert_close(out.cpu().numpy(), ref, f"misaligned {shape} {epi} {path}")
+
+
+# ---------------------------------------------------------------- zero padding
+def tc_supported_pad(ig3, shape, pad, epi):
+    N, Cin, D, H, W, Cout = shape
+    return tc_supported(ig3, N, Cin, D + 2 * pad, H + 2 * pad, W + 2 * pad, Cout, epi)
+
+
+# (N, Cin, D, H, W, Cout, pad): the tensor-core variants the padded shapes select
+# (kd x kw window, split columns, kd window), pad 2, and shapes only FMA takes.
+PAD_CASES = [
+    (1, 8, 4, 9, 62, 16, 1),    # padded W = 64: Cout 16 kd x kw window
+    (2, 16, 5, 7, 30, 32, 1),   # padded W = 32: split hi/lo columns
+    (1, 24, 3, 5, 20, 64, 1),   # kd window, Cin not a multiple of 16
+    (1, 4, 3, 3, 3, 16, 2),     # pad 2, a 3x3x3 input
+    (1, 3, 2, 3, 4, 5, 1),      # D = 2 input (valid conv impossible), odd channels: FMA
+    (2, 5, 1, 1, 1, 16, 1),     # single voxel: one output per channel
+]
+
+
+@pytest.mark.parametrize("case", PAD_CASES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("epi", ["tanh_mish", "none"])
+def test_conv3d_pad_small_all_outputs(ig3, case, epi):
+    *shape, pad = case
+    N, Cin, D, H, W, Cout = shape
+    wl = si.conv3d_workload("t", N, Cin, D, H, W, Cout, seed=3000 + sum(case), epilogue=epi, pad=pad)
+    t = wl.generate_all()
+    y = oracle.conv3d_pad(t["x"], t["w"], t["b"], pad)
+    ref = oracle.tanh_mish(y) if epi == "tanh_mish" else y
+    paths = ["fma"] + (["tc"] if tc_supported_pad(ig3, tuple(shape), pad, epi) else [])
+    for path in paths:
+        x = to_dev(t["x"]); w = to_dev(t["w"]); b = to_dev(t["b"])
+        got = ig3.conv3d_fused(x, w, b, epilogue=epi, path=path, pad=pad)
+        assert ig3.ig3_last_device_status() == 0
+        assert tuple(got.shape) == ref.shape
+        assert_close(got.cpu().numpy(), ref, f"{case} {epi} {path}")
+
+
+@pytest.mark.parametrize("case", [(2, 8, 6, 8, 62, 16, 1), (1, 4, 5, 5, 5, 16, 1)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_conv3d_pad_pool_reduce(ig3, case):
+    *shape, pad = case
+    N, Cin, D, H, W, Cout = shape
+    wl = si.conv3d_workload("t", N, Cin, D, H, W, Cout, seed=3100 + sum(case), epilogue="pool_reduce",
+                            bias2=True, pad=pad)
+    t = wl.generate_all()
+    ref = oracle.pool_reduce(oracle.conv3d_pad(t["x"], t["w"], t["b"], pad), 2.0, 2, t["bias2"])
+    paths = ["fma"] + (["tc"] if tc_supported_pad(ig3, tuple(shape), pad, "pool_reduce") else [])
+    for path in paths:
+        got = ig3.conv3d_fused(to_dev(t["x"]), to_dev(t["w"]), to_dev(t["b"]), epilogue="pool_reduce",
+                               params={"divisor": 2.0, "pool": 2, "bias2": to_dev(t["bias2"])}, path=path, pad=pad)
+        assert ig3.ig3_last_device_status() == 0
+        assert_close(got.cpu().numpy(), ref, f"{case} pool {path}")
+
+
+def test_conv3d_pad_full_size_sampled(ig3):
+    wl = si.conv3d_same_tanh_mish()
+    t = wl.generate_all()
+    x = to_dev(t["x"]); w = to_dev(t["w"]); b = to_dev(t["b"])
+    out = ig3.conv3d_fused(x, w, b, epilogue="tanh_mish", pad=wl.pad)   # the benchmark's call
+    assert ig3.ig3_last_device_status() == 0
+    assert tuple(out.shape) == (16, 64, 32, 64, 64)
+    idx = sample_indices(tuple(out.shape), 6000, seed=61)
+    # Include the faces, edges and corners, where the zero border is read.
+    rng = np.random.default_rng(62)
+    faces = np.stack([rng.integers(0, 16, 600), rng.integers(0, 64, 600),
+                      rng.choice([0, 31], 600), rng.choice([0, 63], 600), rng.integers(0, 64, 600)], 1)
+    idx = np.concatenate([idx, faces])
+    got = out[tuple(torch.from_numpy(idx.T).to(out.device))].cpu().numpy()
+    ref = oracle.tanh_mish(oracle.conv3d_pad_at(t["x"], t["w"], t["b"], wl.pad, idx))
+    assert_close(got, ref, "conv3d pad 1 full size sampled")
+    del x, w, b, out
+    torch.cuda.empty_cache()
