@@ -540,6 +540,35 @@ def run_reference(args) -> None:
     print(json.dumps(line))
 
 
+def run_dwsep_crossover(args) -> None:
+    """Depthwise-separable path study: both paths timed (CUDA events, inputs resident) over
+    a grid of small images and channel counts; one JSON line per shape with the faster
+    path and the one IG3_PATH_AUTO takes."""
+    import torch
+    import implicit_gemm_convolution_x3x3_gb300 as ig3
+    torch.cuda.set_device(0)
+    shapes = [(n, c, hw, hw, co) for (n, hw) in ((1, 32), (1, 64), (2, 128), (4, 256))
+              for c in (16, 32, 64) for co in (16, 32, 64, 128)]
+    for (N, C, H, W, Cout) in shapes:
+        wl = si.dwsep_workload(f"dwsep_{N}x{C}x{H}x{W}_c{Cout}", N, C, H, W, Cout, seed=700 + C + Cout)
+        t = {k: torch.from_numpy(v).cuda() for k, v in wl.generate_all().items()}
+        row = {"study": "dwsep_crossover", "N": N, "C": C, "H": H, "W": W, "Cout": Cout,
+               "gflop": 2.0 * macs(wl) / 1e9,
+               "auto": ig3.dwsep_conv2d_select_path(N, C, H, W, Cout, "auto")}
+        for path in ("tc", "fma"):
+            try:
+                ig3.dwsep_conv2d_select_path(N, C, H, W, Cout, path)
+            except ig3.Ig3Error:
+                row[path + "_us"] = None
+                continue
+            call, _, _ = make_call(ig3, wl, t, path)
+            ms, _, _ = time_steps(call, args.steps, args.warmup, False)
+            row[path + "_us"] = round(1e3 * ms / args.steps, 2)
+        timed = [p for p in ("tc", "fma") if row[p + "_us"] is not None]
+        row["faster"] = min(timed, key=lambda p: row[p + "_us"])
+        print(json.dumps(row), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -551,6 +580,8 @@ def main():
     ap.add_argument("--no-others", action="store_true", help="skip the other workloads' summary")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample size in seconds")
+    ap.add_argument("--study", choices=["dwsep_crossover"], default=None,
+                    help="run a path study instead of the benchmark (JSON line per shape)")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch size (smaller cases for profiling; not a bench line)")
     args = ap.parse_args()
@@ -559,7 +590,9 @@ def main():
         WORKLOADS[args.workload] = lambda: with_batch(base(), args.batch)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.impl == "reference":
+    if args.study == "dwsep_crossover":
+        run_dwsep_crossover(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -122,8 +122,15 @@ int dwsep_select(int N, int C, int H, int W, int Cout, int path) {
     return IG3_PATH_TC;
   }
   if (path == IG3_PATH_FMA) return IG3_PATH_FMA;
-  const double macs = (double)N * H * W * (double)C * (9.0 + Cout);
-  return (tc_ok && macs >= 6.7e7) ? IG3_PATH_TC : IG3_PATH_FMA;
+  if (!tc_ok) return IG3_PATH_FMA;
+  // Per-call cost models (microseconds) fitted to the measured crossover of the two
+  // paths (N 1..4, H = W 32..256, C 16..64, Cout 16..128; one GB300): a fixed part
+  // that grows with the channel counts (both paths are latency-bound at these sizes)
+  // plus the work at each path's large-size rate.
+  const double gflop = 2e-9 * (double)N * H * W * (double)C * (9.0 + Cout);
+  const double t_tc = 8.5 + 0.23 * C + 0.075 * Cout + 6.0 * gflop;
+  const double t_fma = 6.6 + 0.39 * C + 93.0 * gflop;
+  return t_tc < t_fma ? IG3_PATH_TC : IG3_PATH_FMA;
 }
 
 }  // namespace

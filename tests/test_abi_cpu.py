@@ -176,3 +176,16 @@ def test_conv3d_pad_argument_errors(lib):
     # pad 1: the bordered copy [1][2][6][7][8] (256-byte aligned) plus the valid query of that shape
     assert q(1, 2, 4, 5, 6, 1, 16, 1, 1) == \
         (2 * 6 * 7 * 8 * 4 + 255) // 256 * 256 + lib.conv3d_fused_workspace_size(1, 2, 6, 7, 8, 16, 1, 1)
+
+
+def test_dwsep_auto_path_follows_measured_crossover(lib):
+    # Shapes from the measured crossover of the two depthwise-separable paths
+    # (bench.py --study dwsep_crossover): the faster path there is the automatic choice.
+    f = lib.dwsep_conv2d_select_path
+    f.restype = ctypes.c_int
+    TC, FMA = 1, 2
+    assert f(1, 16, 32, 32, 128, 0) == FMA     # tiny, C = 16: FMA 13.9 us, TC 23.5 us
+    assert f(2, 64, 128, 128, 16, 0) == TC     # TC 23.5 us, FMA 33.3 us
+    assert f(1, 64, 64, 64, 32, 0) == TC       # TC 25.2 us, FMA 33.3 us
+    assert f(4, 64, 256, 256, 128, 0) == TC    # TC 60 us, FMA 458 us
+    assert f(1, 24, 64, 64, 32, 0) == FMA      # C not a multiple of 16: no TC kernel
