@@ -15,6 +15,9 @@ Parity status of each function (what pins it; see tests/test_oracle_pins.py):
   conv3d_pad / _at         pinned: np.pad + brute-force im2col, scipy correlate in
                            'same' mode, delta kernel (y = x), constant-input corner and
                            interior closed forms, pad 0 == conv3d.
+  conv3d_ex / _at          pinned: np.pad + strided brute-force im2col, scipy valid
+                           correlation subsampled, centre delta with stride 2 (y =
+                           x[::2]), stride 1 == conv3d_pad, the printed size formula.
   tanh_mish                pinned: algebraic identity form, special values,
                            large-y asymptote, Mish minimum.
   pool_reduce              pinned: window enumeration, S/(div*cells)+sum(bias2)
@@ -71,6 +74,11 @@ def _load():
         lib.oracle_conv3d_pad_at.restype = ctypes.c_double
         lib.oracle_conv3d_pad_at.argtypes = [_fp, _i64, _i64, _i64, _i64, _i64, _i64, _fp, _i64, _fp,
                                              _i64, _i64, _i64, _i64, _i64]
+        lib.oracle_conv3d_ex_at.restype = ctypes.c_double
+        lib.oracle_conv3d_ex_at.argtypes = [_fp, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _fp, _i64, _fp,
+                                            _i64, _i64, _i64, _i64, _i64]
+        lib.oracle_conv3d_ex.restype = None
+        lib.oracle_conv3d_ex.argtypes = [_fp, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _fp, _i64, _fp, _dp]
         lib.oracle_conv3d_pad.restype = None
         lib.oracle_conv3d_pad.argtypes = [_fp, _i64, _i64, _i64, _i64, _i64, _i64, _fp, _i64, _fp, _dp]
         lib.oracle_tanh_mish.restype = ctypes.c_double
@@ -189,6 +197,39 @@ def conv3d_pad_at(x, w, b, pad: int, index) -> np.ndarray:
     for i, (n, k, od, oh, ow) in enumerate(idx):
         out[i] = lib.oracle_conv3d_pad_at(xp, N, Cin, D, H, W, int(pad), wp, Cout, bp,
                                           int(n), int(k), int(od), int(oh), int(ow))
+    return out
+
+
+def conv3d_ex_out_dims(D: int, H: int, W: int, pad: int, stride: int) -> tuple:
+    return tuple((s + 2 * pad - 3) // stride + 1 for s in (D, H, W))
+
+
+def conv3d_ex(x, w, b=None, pad: int = 0, stride: int = 1) -> np.ndarray:
+    """Zero-padded 3x3x3 cross-correlation with stride, float64 [N,Cout,OD,OH,OW]."""
+    lib = _load()
+    x = _f32(x); w = _f32(w); b = None if b is None else _f32(b)
+    N, Cin, D, H, W = x.shape
+    Cout = w.shape[0]
+    assert w.shape == (Cout, Cin, 3, 3, 3) and pad >= 0 and stride >= 1
+    OD, OH, OW = conv3d_ex_out_dims(D, H, W, pad, stride)
+    y = np.empty((N, Cout, max(OD, 0), max(OH, 0), max(OW, 0)), dtype=np.float64)
+    lib.oracle_conv3d_ex(_fptr(x), N, Cin, D, H, W, int(pad), int(stride), _fptr(w), Cout, _fptr(b),
+                         y.ctypes.data_as(_dp))
+    return y
+
+
+def conv3d_ex_at(x, w, b, pad: int, stride: int, index) -> np.ndarray:
+    """Strided, padded conv outputs at a list of (n, k, od, oh, ow) indices (float64)."""
+    lib = _load()
+    x = _f32(x); w = _f32(w); b = None if b is None else _f32(b)
+    N, Cin, D, H, W = x.shape
+    Cout = w.shape[0]
+    idx = np.asarray(index, dtype=np.int64).reshape(-1, 5)
+    out = np.empty(len(idx), dtype=np.float64)
+    xp, wp, bp = _fptr(x), _fptr(w), _fptr(b)
+    for i, (n, k, od, oh, ow) in enumerate(idx):
+        out[i] = lib.oracle_conv3d_ex_at(xp, N, Cin, D, H, W, int(pad), int(stride), wp, Cout, bp,
+                                         int(n), int(k), int(od), int(oh), int(ow))
     return out
 
 

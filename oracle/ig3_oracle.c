@@ -127,6 +127,45 @@ void oracle_conv3d_pad(const float* x, i64 N, i64 Cin, i64 D, i64 H, i64 W, i64 
 }
 
 /*
+ * One output of the zero-padded 3x3x3 cross-correlation with padding P and stride S:
+ *   y[n,k,od,oh,ow] = b[k] + sum_{c,kd,kh,kw} w[k,c,kd,kh,kw] * x[n,c,od*S+kd-P,oh*S+kh-P,ow*S+kw-P]
+ * (zero outside), output size (D + 2P - 3)/S + 1 etc. (integer division).  [P47] the
+ * stride and padding discussion: the input window of output d_out starts at
+ * d_out*stride - padding, and OD = (D + 2*padding - KD)/stride + 1.
+ */
+double oracle_conv3d_ex_at(const float* x, i64 N, i64 Cin, i64 D, i64 H, i64 W, i64 P, i64 S,
+                           const float* w, i64 Cout, const float* b,
+                           i64 n, i64 k, i64 od, i64 oh, i64 ow) {
+  (void)N; (void)Cout;
+  double acc = (b != NULL) ? (double)b[k] : 0.0;
+  for (i64 c = 0; c < Cin; ++c)
+    for (i64 kd = 0; kd < 3; ++kd)
+      for (i64 kh = 0; kh < 3; ++kh)
+        for (i64 kw = 0; kw < 3; ++kw) {
+          const i64 d = od * S + kd - P, h = oh * S + kh - P, ww = ow * S + kw - P;
+          if (d < 0 || d >= D || h < 0 || h >= H || ww < 0 || ww >= W) continue;  /* zero */
+          double xv = (double)x[(((n * Cin + c) * D + d) * H + h) * W + ww];
+          double wv = (double)w[(((k * Cin + c) * 3 + kd) * 3 + kh) * 3 + kw];
+          acc += wv * xv;
+        }
+  return acc;
+}
+
+void oracle_conv3d_ex(const float* x, i64 N, i64 Cin, i64 D, i64 H, i64 W, i64 P, i64 S,
+                      const float* w, i64 Cout, const float* b, double* y) {
+  const i64 OD = (D + 2 * P - 3) / S + 1, OH = (H + 2 * P - 3) / S + 1, OW = (W + 2 * P - 3) / S + 1;
+  if (D + 2 * P < 3 || H + 2 * P < 3 || W + 2 * P < 3) return;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+  for (i64 n = 0; n < N; ++n)
+    for (i64 k = 0; k < Cout; ++k)
+      for (i64 od = 0; od < OD; ++od)
+        for (i64 oh = 0; oh < OH; ++oh)
+          for (i64 ow = 0; ow < OW; ++ow)
+            y[(((n * Cout + k) * OD + od) * OH + oh) * OW + ow] =
+                oracle_conv3d_ex_at(x, N, Cin, D, H, W, P, S, w, Cout, b, n, k, od, oh, ow);
+}
+
+/*
  * out = tanh(mish(y)), mish(y) = y * tanh(softplus(y)), softplus(y) = log(1 + e^y).
  * [P47] the activation description ("PyTorch computes mish first, then tanh").
  * Softplus is evaluated as log1p(exp(y)) with no threshold: for large y, exp

@@ -237,6 +237,78 @@ def test_conv3d_pad_zero_equals_valid_and_at_matches_full():
     assert np.array_equal(oracle.conv3d_pad_at(x, w, b, 1, idx), y[tuple(idx.T)])
 
 
+# ------------------------------------------------------------------ strided conv3d
+# [P47] the stride and padding discussion: input window of output d_out starts at
+# d_out*stride - padding; OD = (D + 2*padding - KD)/stride + 1.
+def strided_im2col(xp, w, b, S):
+    """Brute force on an already padded input: strided [M x K] patches times W^T (float64)."""
+    xp = xp.astype(np.float64); w = w.astype(np.float64)
+    N, Cin, D, H, W = xp.shape
+    Cout = w.shape[0]
+    OD, OH, OW = (D - 3) // S + 1, (H - 3) // S + 1, (W - 3) // S + 1
+    cols = np.empty((N, OD, OH, OW, Cin, 3, 3, 3))
+    for kd in range(3):
+        for kh in range(3):
+            for kw in range(3):
+                patch = xp[:, :, kd:kd + S * (OD - 1) + 1:S, kh:kh + S * (OH - 1) + 1:S,
+                           kw:kw + S * (OW - 1) + 1:S]
+                cols[..., kd, kh, kw] = np.moveaxis(patch, 1, -1)
+    Y = cols.reshape(N * OD * OH * OW, Cin * 27) @ w.reshape(Cout, Cin * 27).T
+    if b is not None:
+        Y = Y + b.astype(np.float64)[None, :]
+    return np.moveaxis(Y.reshape(N, OD, OH, OW, Cout), -1, 1)
+
+
+@pytest.mark.parametrize("shape,pad,stride", [((1, 2, 5, 6, 7, 3), 0, 2), ((2, 3, 6, 5, 8, 2), 1, 2),
+                                              ((1, 2, 4, 4, 4, 2), 2, 2), ((1, 1, 3, 3, 3, 1), 0, 2),
+                                              ((1, 2, 7, 9, 6, 2), 1, 3), ((1, 2, 4, 5, 6, 2), 1, 1)])
+def test_conv3d_ex_vs_numpy_pad_and_strided_im2col(shape, pad, stride):
+    N, Cin, D, H, W, Cout = shape
+    rng = np.random.default_rng(200 + sum(shape) + 7 * pad + stride)
+    x = rng.standard_normal((N, Cin, D, H, W)).astype(np.float32)
+    w = rng.uniform(-1, 1, (Cout, Cin, 3, 3, 3)).astype(np.float32)
+    b = rng.uniform(-1, 1, Cout).astype(np.float32)
+    xp = np.pad(x, ((0, 0), (0, 0), (pad, pad), (pad, pad), (pad, pad)))
+    y = oracle.conv3d_ex(x, w, b, pad, stride)
+    assert y.shape[2:] == tuple((s + 2 * pad - 3) // stride + 1 for s in (D, H, W))
+    assert rel_err(y, strided_im2col(xp, w, b, stride)) < 1e-12
+
+
+def test_conv3d_ex_vs_scipy_valid_subsampled():
+    rng = np.random.default_rng(201)
+    x = rng.standard_normal((1, 2, 7, 8, 9)).astype(np.float32)
+    w = rng.uniform(-1, 1, (2, 2, 3, 3, 3)).astype(np.float32)
+    xp = np.pad(x, ((0, 0), (0, 0), (1, 1), (1, 1), (1, 1))).astype(np.float64)
+    ref = np.zeros((1, 2) + tuple((s + 2 - 3) // 2 + 1 for s in (7, 8, 9)))
+    for k in range(2):
+        full = sum(scipy.signal.correlate(xp[0, c], w[k, c].astype(np.float64), mode="valid", method="direct")
+                   for c in range(2))
+        ref[0, k] = full[::2, ::2, ::2]
+    assert rel_err(oracle.conv3d_ex(x, w, None, 1, 2), ref) < 1e-12
+
+
+def test_conv3d_ex_centre_delta_subsamples():
+    rng = np.random.default_rng(202)
+    C = 2
+    x = rng.standard_normal((1, C, 7, 6, 5)).astype(np.float32)
+    w = np.zeros((C, C, 3, 3, 3), np.float32)
+    for k in range(C):
+        w[k, k, 1, 1, 1] = 1.0
+    # pad 1, stride 2: output (od, oh, ow) reads x[2od, 2oh, 2ow]
+    assert np.array_equal(oracle.conv3d_ex(x, w, None, 1, 2), x[:, :, ::2, ::2, ::2].astype(np.float64))
+
+
+def test_conv3d_ex_stride1_is_padded_and_at_matches_full():
+    rng = np.random.default_rng(203)
+    x = rng.standard_normal((1, 2, 5, 6, 7)).astype(np.float32)
+    w = rng.uniform(-1, 1, (2, 2, 3, 3, 3)).astype(np.float32)
+    b = rng.uniform(-1, 1, 2).astype(np.float32)
+    assert np.array_equal(oracle.conv3d_ex(x, w, b, 1, 1), oracle.conv3d_pad(x, w, b, 1))
+    y = oracle.conv3d_ex(x, w, b, 1, 2)
+    idx = np.stack([rng.integers(0, s, 30) for s in y.shape], 1)
+    assert np.array_equal(oracle.conv3d_ex_at(x, w, b, 1, 2, idx), y[tuple(idx.T)])
+
+
 # ------------------------------------------------------------------ tanh(mish)
 def test_tanh_mish_zero():
     assert oracle.tanh_mish_scalar(0.0) == 0.0
