@@ -55,6 +55,7 @@ WORKLOADS = {
     "sweep128": lambda: si.conv3d_sweep(128),
     "tiny": si.tiny_conv3d,
     "conv3d_same": si.conv3d_same_tanh_mish,
+    "conv3d_s2": si.conv3d_stride2_tanh_mish,
 }
 
 
@@ -68,8 +69,8 @@ def with_batch(wl, n: int):
 
 # ------------------------------------------------------------------ workload arithmetic
 def conv_out_dims(wl) -> tuple:
-    d, p = wl.dims, wl.pad
-    return d["D"] + 2 * p - 2, d["H"] + 2 * p - 2, d["W"] + 2 * p - 2
+    d, p, s = wl.dims, wl.pad, wl.stride
+    return tuple((d[k] + 2 * p - 3) // s + 1 for k in ("D", "H", "W"))
 
 
 def macs(wl) -> int:
@@ -101,7 +102,7 @@ def describe(wl) -> str:
         epi = {"tanh_mish": "tanh(mish)", "pool_reduce": "/2-maxpool2-mean-+bias2-sum_c",
                "none": "none"}[wl.epilogue]
         kind = f"pad{wl.pad}" if wl.pad else "valid"
-        return (f"conv3d k3 {kind} s1 x[{d['N']},{d['Cin']},{d['D']},{d['H']},{d['W']}] "
+        return (f"conv3d k3 {kind} s{wl.stride} x[{d['N']},{d['Cin']},{d['D']},{d['H']},{d['W']}] "
                 f"w[{d['Cout']},{d['Cin']},3,3,3] epilogue {epi}")
     return (f"dwsep conv2d x[{d['N']},{d['C']},{d['H']},{d['W']}] dw 3x3 pad1 -> pw "
             f"{d['C']}->{d['Cout']}, no bias")
@@ -237,15 +238,18 @@ def make_call(ig3, wl, dev_t: dict, path: str):
         else:
             out = torch.empty((d["N"], d["Cout"]) + conv_out_dims(wl), device=dev_t["x"].device)
         p2 = 2 * wl.pad
-        need = ig3.conv3d_fused_pad_workspace_size(d["N"], d["Cin"], d["D"], d["H"], d["W"], wl.pad, d["Cout"],
-                                                   wl.epilogue, path)
+        if wl.stride == 1:
+            need = ig3.conv3d_fused_pad_workspace_size(d["N"], d["Cin"], d["D"], d["H"], d["W"], wl.pad, d["Cout"],
+                                                       wl.epilogue, path)
+            chosen = ig3.conv3d_fused_select_path(d["N"], d["Cin"], d["D"] + p2, d["H"] + p2, d["W"] + p2,
+                                                  d["Cout"], wl.epilogue, path)
+        else:
+            need, chosen = 0, "fma"   # strided: the FMA kernel, no workspace
         ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev_t["x"].device)
-        chosen = ig3.conv3d_fused_select_path(d["N"], d["Cin"], d["D"] + p2, d["H"] + p2, d["W"] + p2, d["Cout"],
-                                              wl.epilogue, path)
 
         def call():
             ig3.conv3d_fused(dev_t["x"], dev_t["w"], dev_t.get("b"), epilogue=wl.epilogue, params=params, out=out,
-                             workspace=ws, path=path, pad=wl.pad)
+                             workspace=ws, path=path, pad=wl.pad, stride=wl.stride)
         return call, out, chosen
     d = wl.dims
     out = torch.empty((d["N"], d["Cout"], d["H"], d["W"]), device=dev_t["x"].device)
@@ -391,11 +395,13 @@ def oracle_sample(wl, target_s: float):
         _, oh, ow = conv_out_dims(wl)
 
         def make(planes):
-            xs = np.ascontiguousarray(t["x"][0:1, :, 0:planes + 2 - 2 * wl.pad])
+            # input planes that the first `planes` output planes read (the slab's far
+            # end then reads the zero border: the same work, for timing)
+            xs = np.ascontiguousarray(t["x"][0:1, :, 0:max(1, (planes - 1) * wl.stride + 3 - 2 * wl.pad)])
 
             def run():
                 t0 = time.perf_counter()
-                y = oracle.conv3d_pad(xs, t["w"], t.get("b"), wl.pad)
+                y = oracle.conv3d_ex(xs, t["w"], t.get("b"), wl.pad, wl.stride)
                 if wl.epilogue == "tanh_mish":
                     oracle.tanh_mish(y)
                 elif wl.epilogue == "pool_reduce":
@@ -461,7 +467,8 @@ def run_ours(args) -> None:
 
     others = []
     if rank == 0 and not args.no_others and world == 1:
-        for name in ["tiny", "conv3d_pool_reduce", "dwsep", "sweep16", "sweep64", "sweep128", "conv3d_same"]:
+        for name in ["tiny", "conv3d_pool_reduce", "dwsep", "sweep16", "sweep64", "sweep128", "conv3d_same",
+                     "conv3d_s2"]:
             if name == args.workload:
                 continue
             owl = WORKLOADS[name]()

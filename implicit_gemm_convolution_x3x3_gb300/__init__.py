@@ -60,6 +60,8 @@ _SIGS = {
     "dwsep_conv2d": (_i, [_p, _i, _i, _i, _i, _p, _p, _i, _p, _p, _i, _p]),
     "conv3d_fused_pad_workspace_size": (ctypes.c_size_t, [_i] * 9),
     "conv3d_fused_pad": (_i, [_p, _i, _i, _i, _i, _i, _i, _p, _i, _p, _i, _p, _p, _p, ctypes.c_size_t, _i, _p]),
+    "conv3d_fused_ex_workspace_size": (ctypes.c_size_t, [_i] * 10),
+    "conv3d_fused_ex": (_i, [_p, _i, _i, _i, _i, _i, _i, _i, _p, _i, _p, _i, _p, _p, _p, ctypes.c_size_t, _i, _p]),
     "conv3d_fused_select_path": (_i, [_i] * 8),
     "dwsep_conv2d_select_path": (_i, [_i] * 6),
     "ig3_status_string": (ctypes.c_char_p, [_i]),
@@ -166,14 +168,15 @@ def conv3d_fused_pad_workspace_size(N, Cin, D, H, W, pad, Cout, epilogue="tanh_m
 
 def conv3d_fused(x: torch.Tensor, w: torch.Tensor, b: torch.Tensor | None = None, epilogue="tanh_mish",
                  params: dict | None = None, out: torch.Tensor | None = None,
-                 workspace: torch.Tensor | None = None, path="auto", stream=None, pad: int = 0) -> torch.Tensor:
-    """Stride-1 3x3x3 conv3d with a fused epilogue (see include/ig3.h): valid, or
-    zero-padded by ``pad`` on every side (conv3d_fused_pad).
+                 workspace: torch.Tensor | None = None, path="auto", stream=None, pad: int = 0,
+                 stride: int = 1) -> torch.Tensor:
+    """3x3x3 conv3d with a fused epilogue (see include/ig3.h): valid, zero-padded by
+    ``pad`` on every side (conv3d_fused_pad), or with stride 2 (conv3d_fused_ex).
 
     ``params`` (POOL_REDUCE only): ``{"divisor": 2.0, "pool": 2, "bias2": tensor[Cout]}``.
-    Returns ``out`` ([N,Cout,D+2*pad-2,H+2*pad-2,W+2*pad-2], or [N] for POOL_REDUCE).
+    Returns ``out`` ([N,Cout,OD,OH,OW] with OD = (D+2*pad-3)//stride+1, or [N] for POOL_REDUCE).
     """
-    pad = int(pad)
+    pad, stride = int(pad), int(stride)
     epi = _enum(EPILOGUES, epilogue, "epilogue")
     pth = _enum(PATHS, path, "path")
     if x.dim() != 5 or w.dim() != 5:
@@ -192,12 +195,14 @@ def conv3d_fused(x: torch.Tensor, w: torch.Tensor, b: torch.Tensor | None = None
                         _dev_f32(params["bias2"], "bias2", (Cout,)))
         oshape = (N,)
     else:
-        oshape = (N, Cout, D + 2 * pad - 2, H + 2 * pad - 2, W + 2 * pad - 2)
+        oshape = (N, Cout) + tuple((s + 2 * pad - 3) // stride + 1 for s in (D, H, W))
     if out is None:
         out = torch.empty(oshape, dtype=torch.float32, device=x.device)
     yp = _dev_f32(out, "out", oshape)
     with torch.cuda.device(x.device):
-        if pad == 0:
+        if stride != 1:
+            need = int(lib.conv3d_fused_ex_workspace_size(N, Cin, D, H, W, pad, stride, Cout, epi, pth))
+        elif pad == 0:
             need = int(lib.conv3d_fused_workspace_size(N, Cin, D, H, W, Cout, epi, pth))
         else:
             need = int(lib.conv3d_fused_pad_workspace_size(N, Cin, D, H, W, pad, Cout, epi, pth))
@@ -206,7 +211,10 @@ def conv3d_fused(x: torch.Tensor, w: torch.Tensor, b: torch.Tensor | None = None
         wsp = None if workspace is None else workspace.data_ptr()
         wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
         epp = None if pr is None else ctypes.byref(pr)
-        if pad == 0:
+        if stride != 1:
+            st = lib.conv3d_fused_ex(xp, N, Cin, D, H, W, pad, stride, wp, Cout, bp, epi, epp, yp, wsp, wsb, pth,
+                                     _stream_handle(stream, x.device))
+        elif pad == 0:
             st = lib.conv3d_fused(xp, N, Cin, D, H, W, wp, Cout, bp, epi, epp, yp, wsp, wsb, pth,
                                   _stream_handle(stream, x.device))
         else:

@@ -126,6 +126,29 @@ int conv3d_fused_pad(const float* x, int N, int Cin, int D, int H, int W, int pa
                      float* y, void* workspace, size_t workspace_bytes,
                      int path, void* stream);
 
+/*
+ * 3x3x3 cross-correlation with zero padding `pad` and stride `stride`, fused epilogue
+ * ([P47], the stride and padding discussion: the input window of output od starts at
+ * od*stride - pad, reads outside the tensor give zero, the output size is
+ * (D + 2*pad - 3)/stride + 1 in integer division):
+ *   conv[n,k,od,oh,ow] = b[k] + sum_{c,kd,kh,kw} w[k,c,kd,kh,kw]
+ *                               * x[n,c,od*stride+kd-pad, oh*stride+kh-pad, ow*stride+kw-pad]
+ *   y   [N][Cout][OD][OH][OW] with OD = (D + 2*pad - 3)/stride + 1 etc.
+ * stride 1: exactly conv3d_fused_pad (every epilogue and path, its workspace).
+ * stride 2: the FP32-FMA path only (IG3_PATH_AUTO or IG3_PATH_FMA; IG3_PATH_TC and the
+ *           POOL_REDUCE epilogue return IG3_ERR_UNSUPPORTED), pad 0..16, no workspace
+ *           (workspace may be NULL; the size query returns 0), and N * ceil(Cout/16)
+ *           and OD at most 65535.
+ * Other strides return IG3_ERR_UNSUPPORTED.  Other arguments as conv3d_fused.
+ */
+size_t conv3d_fused_ex_workspace_size(int N, int Cin, int D, int H, int W, int pad, int stride,
+                                      int Cout, int epilogue, int path);
+int conv3d_fused_ex(const float* x, int N, int Cin, int D, int H, int W, int pad, int stride,
+                    const float* w, int Cout, const float* b,
+                    int epilogue, const ig3_epi_params* params,
+                    float* y, void* workspace, size_t workspace_bytes,
+                    int path, void* stream);
+
 /* Size of the library's own scratch buffer used by conv3d_fused_noalloc (4 MiB). */
 #define IG3_NOALLOC_SCRATCH_BYTES (4u * 1024u * 1024u)
 

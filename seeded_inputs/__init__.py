@@ -117,6 +117,7 @@ class Workload:
     divisor: float = 2.0         # pool_reduce only
     pool: int = 2                # pool_reduce only
     pad: int = 0                 # conv3d only: zero padding on every side
+    stride: int = 1              # conv3d only
 
     def spec(self, name: str) -> TensorSpec:
         for t in self.tensors:
@@ -158,7 +159,7 @@ NORMAL = ("normal",)
 
 
 def conv3d_workload(name, N, Cin, D, H, W, Cout, seed, epilogue="tanh_mish",
-                    x_dist=NORMAL, with_bias=True, bias2=False, wb_bound=None, pad=0) -> Workload:
+                    x_dist=NORMAL, with_bias=True, bias2=False, wb_bound=None, pad=0, stride=1) -> Workload:
     """Conv3d workload: x ~ x_dist, w and b ~ U(+-1/sqrt(27*Cin)) unless wb_bound given."""
     a = wb_bound if wb_bound is not None else 1.0 / math.sqrt(27.0 * Cin)
     ts = [TensorSpec("x", (N, Cin, D, H, W), x_dist),
@@ -167,7 +168,7 @@ def conv3d_workload(name, N, Cin, D, H, W, Cout, seed, epilogue="tanh_mish",
         ts.append(TensorSpec("b", (Cout,), _u(a)))
     if bias2:
         ts.append(TensorSpec("bias2", (Cout,), NORMAL))
-    return Workload(name=name, op="conv3d", seed=seed, tensors=ts, epilogue=epilogue, pad=pad)
+    return Workload(name=name, op="conv3d", seed=seed, tensors=ts, epilogue=epilogue, pad=pad, stride=stride)
 
 
 def dwsep_workload(name, N, C, H, W, Cout, seed, x_dist=NORMAL, with_bias=False) -> Workload:
@@ -217,6 +218,13 @@ def conv3d_same_tanh_mish() -> Workload:
                            seed=6, epilogue="tanh_mish", pad=1)
 
 
+def conv3d_stride2_tanh_mish() -> Workload:
+    """The conv3d + tanh(mish) input with padding 1 and stride 2 (output [16,64,16,32,32]); seed 7."""
+    return conv3d_workload("conv3d_s2_tanh_mish_16x32x32x64x64_c64", 16, 32, 32, 64, 64, 64,
+                           seed=7, epilogue="tanh_mish", pad=1, stride=2)
+
+
 def all_workloads() -> list:
     return [tiny_conv3d(), conv3d_tanh_mish(), conv3d_pool_reduce(), dwsep_conv2d(),
-            conv3d_sweep(16), conv3d_sweep(64), conv3d_sweep(128), conv3d_same_tanh_mish()]
+            conv3d_sweep(16), conv3d_sweep(64), conv3d_sweep(128), conv3d_same_tanh_mish(),
+            conv3d_stride2_tanh_mish()]

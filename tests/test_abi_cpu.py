@@ -189,3 +189,25 @@ def test_dwsep_auto_path_follows_measured_crossover(lib):
     assert f(1, 64, 64, 64, 32, 0) == TC       # TC 25.2 us, FMA 33.3 us
     assert f(4, 64, 256, 256, 128, 0) == TC    # TC 60 us, FMA 458 us
     assert f(1, 24, 64, 64, 32, 0) == FMA      # C not a multiple of 16: no TC kernel
+
+
+def test_conv3d_ex_argument_errors(lib):
+    f = lib.conv3d_fused_ex
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] + [ctypes.c_int] * 7 + [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                                                           ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                                           ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int,
+                                                           ctypes.c_void_p]
+    q = lib.conv3d_fused_ex_workspace_size
+    q.restype = ctypes.c_size_t
+    args = lambda D, pad, stride, Cout, epi, path, x=FAKE: (x, 1, 2, D, D, D, pad, stride, FAKE, Cout, None, epi,
+                                                          None, FAKE, None, 0, path, None)
+    assert f(*args(5, 1, 3, 4, 1, 0)) == -2       # stride 3: not built
+    assert f(*args(5, 1, 0, 4, 1, 0)) == -2       # stride 0
+    assert f(*args(5, -1, 2, 4, 1, 0)) == -1      # negative pad
+    assert f(*args(5, 1, 2, 4, 2, 0)) == -2       # stride 2 with pool-reduce
+    assert f(*args(5, 1, 2, 16, 1, 1)) == -2      # stride 2 on the TC path
+    assert f(*args(2, 0, 2, 4, 1, 0)) == -2       # no output (D + 2*pad < 3)
+    assert f(*args(5, 1, 2, 4, 1, 0, None)) == -1  # NULL x
+    assert q(1, 2, 5, 5, 5, 1, 2, 4, 1, 0) == 0   # stride 2 needs no workspace
+    assert q(1, 2, 5, 5, 5, 1, 1, 16, 1, 1) == lib.conv3d_fused_pad_workspace_size(1, 2, 5, 5, 5, 1, 16, 1, 1)

@@ -314,3 +314,50 @@ def test_conv3d_pad_full_size_sampled(ig3):
     assert_close(got, ref, "conv3d pad 1 full size sampled")
     del x, w, b, out
     torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------- stride 2 (FMA path)
+# (N, Cin, D, H, W, Cout, pad): ragged tiles in every dim, Cout not a multiple of the
+# 16-channel block, odd and even input sizes, pad 0..2.
+STRIDE2_CASES = [
+    (1, 3, 7, 9, 11, 5, 0),
+    (2, 4, 8, 20, 70, 16, 1),
+    (1, 2, 5, 6, 5, 33, 1),
+    (1, 5, 4, 4, 4, 8, 2),
+    (1, 1, 3, 3, 3, 1, 0),      # one output
+]
+
+
+@pytest.mark.parametrize("case", STRIDE2_CASES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("epi", ["tanh_mish", "none"])
+def test_conv3d_stride2_all_outputs(ig3, case, epi):
+    *shape, pad = case
+    N, Cin, D, H, W, Cout = shape
+    wl = si.conv3d_workload("t", N, Cin, D, H, W, Cout, seed=3200 + sum(case), epilogue=epi, pad=pad)
+    t = wl.generate_all()
+    y = oracle.conv3d_ex(t["x"], t["w"], t["b"], pad, 2)
+    ref = oracle.tanh_mish(y) if epi == "tanh_mish" else y
+    for path in ("auto", "fma"):
+        got = ig3.conv3d_fused(to_dev(t["x"]), to_dev(t["w"]), to_dev(t["b"]), epilogue=epi, path=path,
+                               pad=pad, stride=2)
+        assert ig3.ig3_last_device_status() == 0
+        assert tuple(got.shape) == ref.shape
+        assert_close(got.cpu().numpy(), ref, f"{case} {epi} {path}")
+    got = ig3.conv3d_fused(to_dev(t["x"]), to_dev(t["w"]), None, epilogue=epi, pad=pad, stride=2)
+    y0 = oracle.conv3d_ex(t["x"], t["w"], None, pad, 2)
+    assert_close(got.cpu().numpy(), oracle.tanh_mish(y0) if epi == "tanh_mish" else y0, f"{case} no bias")
+
+
+def test_conv3d_stride2_full_size_sampled(ig3):
+    wl = si.conv3d_stride2_tanh_mish()
+    t = wl.generate_all()
+    x = to_dev(t["x"]); w = to_dev(t["w"]); b = to_dev(t["b"])
+    out = ig3.conv3d_fused(x, w, b, epilogue="tanh_mish", pad=wl.pad, stride=wl.stride)   # the benchmark's call
+    assert ig3.ig3_last_device_status() == 0
+    assert tuple(out.shape) == (16, 64, 16, 32, 32)
+    idx = sample_indices(tuple(out.shape), 6000, seed=71)
+    got = out[tuple(torch.from_numpy(idx.T).to(out.device))].cpu().numpy()
+    ref = oracle.tanh_mish(oracle.conv3d_ex_at(t["x"], t["w"], t["b"], wl.pad, wl.stride, idx))
+    assert_close(got, ref, "conv3d stride 2 full size sampled")
+    del x, w, b, out
+    torch.cuda.empty_cache()
