@@ -24,6 +24,8 @@ Parity status of each function (what pins it; see tests/test_oracle_pins.py):
                            identity, constant input, floor mode, planted maxima.
   dwsep / dwsep_single_sum pinned: scipy correlate2d + einsum, two-stage ==
                            single-sum, centre-delta and identity special cases.
+  dwsep_k / dwsep_k_at     pinned: scipy correlate2d 'same' + einsum for K = 1, 3, 5,
+                           7, two-stage == single-sum, K = 3 == dwsep, centre delta.
 """
 from __future__ import annotations
 
@@ -79,6 +81,11 @@ def _load():
                                             _i64, _i64, _i64, _i64, _i64]
         lib.oracle_conv3d_ex.restype = None
         lib.oracle_conv3d_ex.argtypes = [_fp, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _fp, _i64, _fp, _dp]
+        lib.oracle_dwsep_k.restype = ctypes.c_int
+        lib.oracle_dwsep_k.argtypes = [_fp, _i64, _i64, _i64, _i64, _i64, _fp, _fp, _i64, _fp, _dp]
+        lib.oracle_dwsep_k_at.restype = ctypes.c_double
+        lib.oracle_dwsep_k_at.argtypes = [_fp, _i64, _i64, _i64, _i64, _i64, _fp, _fp, _i64, _fp,
+                                          _i64, _i64, _i64, _i64]
         lib.oracle_conv3d_pad.restype = None
         lib.oracle_conv3d_pad.argtypes = [_fp, _i64, _i64, _i64, _i64, _i64, _i64, _fp, _i64, _fp, _dp]
         lib.oracle_tanh_mish.restype = ctypes.c_double
@@ -291,6 +298,36 @@ def dwsep_single_sum(x, w_dw, w_pw, b=None) -> np.ndarray:
     out = np.empty((N, Cout, H, W), dtype=np.float64)
     lib.oracle_dwsep_single_sum(_fptr(x), N, C, H, W, _fptr(w_dw), _fptr(w_pw), Cout, _fptr(b),
                                 out.ctypes.data_as(_dp))
+    return out
+
+
+def dwsep_k(x, w_dw, w_pw, b=None) -> np.ndarray:
+    """Depthwise KxK ("same" padding (K-1)/2, K odd) then pointwise 1x1, two-stage, float64."""
+    lib = _load()
+    x = _f32(x); w_dw = _f32(w_dw); w_pw = _f32(w_pw); b = None if b is None else _f32(b)
+    N, C, H, W = x.shape
+    K = w_dw.shape[-1]
+    Cout = w_pw.shape[0]
+    assert w_dw.shape == (C, 1, K, K) and K % 2 == 1 and w_pw.shape == (Cout, C, 1, 1)
+    out = np.empty((N, Cout, H, W), dtype=np.float64)
+    if lib.oracle_dwsep_k(_fptr(x), N, C, H, W, K, _fptr(w_dw), _fptr(w_pw), Cout, _fptr(b),
+                          out.ctypes.data_as(_dp)) != 0:
+        raise MemoryError("oracle_dwsep_k could not allocate its depthwise stage")
+    return out
+
+
+def dwsep_k_at(x, w_dw, w_pw, b, index) -> np.ndarray:
+    """dwsep_k outputs at a list of (n, o, h, w) indices (single-sum form, float64)."""
+    lib = _load()
+    x = _f32(x); w_dw = _f32(w_dw); w_pw = _f32(w_pw); b = None if b is None else _f32(b)
+    N, C, H, W = x.shape
+    K = w_dw.shape[-1]
+    Cout = w_pw.shape[0]
+    idx = np.asarray(index, dtype=np.int64).reshape(-1, 4)
+    out = np.empty(len(idx), dtype=np.float64)
+    xp, dp_, pp, bp = _fptr(x), _fptr(w_dw), _fptr(w_pw), _fptr(b)
+    for i, (n, o, h, w) in enumerate(idx):
+        out[i] = lib.oracle_dwsep_k_at(xp, N, C, H, W, K, dp_, pp, Cout, bp, int(n), int(o), int(h), int(w))
     return out
 
 

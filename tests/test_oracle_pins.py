@@ -494,3 +494,39 @@ def test_dwsep_at_matches_full():
     idx = np.stack([rng.integers(0, s, 60) for s in full.shape], 1)
     got = oracle.dwsep_at(t["x"], t["w_dw"], t["w_pw"], None, idx)
     assert rel_err(got, full[tuple(idx.T)]) < 1e-14
+
+
+# ------------------------------------------------------------------ dwsep, K x K
+# [P86] the discussion of kernel sizes other than 3 (templated on K, dispatched for 1,
+# 3, 5, 7); reading: stride 1, dilation 1, padding (K-1)/2.
+@pytest.mark.parametrize("K", [1, 3, 5, 7])
+def test_dwsep_k_vs_scipy_same_and_einsum(K):
+    rng = np.random.default_rng(300 + K)
+    N, C, H, W, Cout = 2, 3, 9, 8, 4
+    x = rng.standard_normal((N, C, H, W)).astype(np.float32)
+    w_dw = rng.uniform(-1, 1, (C, 1, K, K)).astype(np.float32)
+    w_pw = rng.uniform(-1, 1, (Cout, C, 1, 1)).astype(np.float32)
+    b = rng.uniform(-1, 1, Cout).astype(np.float32)
+    dw = np.zeros((N, C, H, W))
+    for n in range(N):
+        for c in range(C):
+            dw[n, c] = scipy.signal.correlate2d(x[n, c].astype(np.float64), w_dw[c, 0].astype(np.float64),
+                                                mode="same", boundary="fill")
+    ref = np.einsum("oc,nchw->nohw", w_pw[:, :, 0, 0].astype(np.float64), dw) + b[None, :, None, None]
+    got = oracle.dwsep_k(x, w_dw, w_pw, b)
+    assert rel_err(got, ref) < 1e-12
+    idx = np.stack([rng.integers(0, s, 40) for s in got.shape], 1)
+    assert rel_err(oracle.dwsep_k_at(x, w_dw, w_pw, b, idx), got[tuple(idx.T)]) < 1e-12
+
+
+def test_dwsep_k3_equals_dwsep_and_centre_delta():
+    rng = np.random.default_rng(310)
+    x = rng.standard_normal((1, 3, 7, 6)).astype(np.float32)
+    w3 = rng.uniform(-1, 1, (3, 1, 3, 3)).astype(np.float32)
+    w_pw = rng.uniform(-1, 1, (2, 3, 1, 1)).astype(np.float32)
+    assert np.array_equal(oracle.dwsep_k(x, w3, w_pw), oracle.dwsep(x, w3, w_pw))
+    w5 = np.zeros((3, 1, 5, 5), np.float32)
+    w5[:, 0, 2, 2] = 1.0        # centre tap: the depthwise stage is the identity
+    ref = np.einsum("oc,nchw->nohw", w_pw[:, :, 0, 0].astype(np.float64), x.astype(np.float64))
+    assert rel_err(oracle.dwsep_k(x, w5, w_pw), ref) < 1e-14
+
