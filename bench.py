@@ -56,6 +56,7 @@ WORKLOADS = {
     "tiny": si.tiny_conv3d,
     "conv3d_same": si.conv3d_same_tanh_mish,
     "conv3d_s2": si.conv3d_stride2_tanh_mish,
+    "dwsep_k5": si.dwsep_k5,
 }
 
 
@@ -78,7 +79,7 @@ def macs(wl) -> int:
     if wl.op == "conv3d":
         od, oh, ow = conv_out_dims(wl)
         return d["N"] * d["Cout"] * od * oh * ow * d["Cin"] * 27
-    return d["N"] * d["H"] * d["W"] * d["C"] * (9 + d["Cout"])
+    return d["N"] * d["H"] * d["W"] * d["C"] * (d["K"] * d["K"] + d["Cout"])
 
 
 def compulsory_bytes(wl) -> tuple:
@@ -104,7 +105,7 @@ def describe(wl) -> str:
         kind = f"pad{wl.pad}" if wl.pad else "valid"
         return (f"conv3d k3 {kind} s{wl.stride} x[{d['N']},{d['Cin']},{d['D']},{d['H']},{d['W']}] "
                 f"w[{d['Cout']},{d['Cin']},3,3,3] epilogue {epi}")
-    return (f"dwsep conv2d x[{d['N']},{d['C']},{d['H']},{d['W']}] dw 3x3 pad1 -> pw "
+    return (f"dwsep conv2d x[{d['N']},{d['C']},{d['H']},{d['W']}] dw {d['K']}x{d['K']} pad{(d['K'] - 1) // 2} -> pw "
             f"{d['C']}->{d['Cout']}, no bias")
 
 
@@ -253,7 +254,8 @@ def make_call(ig3, wl, dev_t: dict, path: str):
         return call, out, chosen
     d = wl.dims
     out = torch.empty((d["N"], d["Cout"], d["H"], d["W"]), device=dev_t["x"].device)
-    chosen = ig3.dwsep_conv2d_select_path(d["N"], d["C"], d["H"], d["W"], d["Cout"], path)
+    # K != 3 runs on the FMA kernel only
+    chosen = ig3.dwsep_conv2d_select_path(d["N"], d["C"], d["H"], d["W"], d["Cout"], path) if d["K"] == 3 else "fma"
 
     def call():
         ig3.dwsep_conv2d(dev_t["x"], dev_t["w_dw"], dev_t["w_pw"], dev_t.get("b"), out=out, path=path)
@@ -420,9 +422,9 @@ def oracle_sample(wl, target_s: float):
 
         def run():
             t0 = time.perf_counter()
-            oracle.dwsep(xs, t["w_dw"], t["w_pw"], t.get("b"))
+            oracle.dwsep_k(xs, t["w_dw"], t["w_pw"], t.get("b"))
             return time.perf_counter() - t0
-        return run, 2.0 * rows * d["W"] * d["C"] * (9 + d["Cout"])
+        return run, 2.0 * rows * d["W"] * d["C"] * (d["K"] * d["K"] + d["Cout"])
     one, _ = make(8)
     dt = one()
     rows = int(max(8, min(d["H"], 8 * target_s / max(dt, 1e-3))))
@@ -468,7 +470,7 @@ def run_ours(args) -> None:
     others = []
     if rank == 0 and not args.no_others and world == 1:
         for name in ["tiny", "conv3d_pool_reduce", "dwsep", "sweep16", "sweep64", "sweep128", "conv3d_same",
-                     "conv3d_s2"]:
+                     "conv3d_s2", "dwsep_k5"]:
             if name == args.workload:
                 continue
             owl = WORKLOADS[name]()

@@ -62,6 +62,7 @@ _SIGS = {
     "conv3d_fused_pad": (_i, [_p, _i, _i, _i, _i, _i, _i, _p, _i, _p, _i, _p, _p, _p, ctypes.c_size_t, _i, _p]),
     "conv3d_fused_ex_workspace_size": (ctypes.c_size_t, [_i] * 10),
     "conv3d_fused_ex": (_i, [_p, _i, _i, _i, _i, _i, _i, _i, _p, _i, _p, _i, _p, _p, _p, ctypes.c_size_t, _i, _p]),
+    "dwsep_conv2d_ex": (_i, [_p, _i, _i, _i, _i, _i, _p, _p, _i, _p, _p, _i, _p]),
     "conv3d_fused_select_path": (_i, [_i] * 8),
     "dwsep_conv2d_select_path": (_i, [_i] * 6),
     "ig3_status_string": (ctypes.c_char_p, [_i]),
@@ -266,21 +267,26 @@ def conv3d_fused_noalloc(x: torch.Tensor, w: torch.Tensor, b: torch.Tensor | Non
 
 def dwsep_conv2d(x: torch.Tensor, w_dw: torch.Tensor, w_pw: torch.Tensor, b: torch.Tensor | None = None,
                  out: torch.Tensor | None = None, path="auto", stream=None) -> torch.Tensor:
-    """Depthwise 3x3 (pad 1) then pointwise 1x1 conv2d (see include/ig3.h); returns [N,Cout,H,W]."""
+    """Depthwise KxK ("same" padding (K-1)/2; K = w_dw.shape[-1], 3 by the source problem)
+    then pointwise 1x1 conv2d (see include/ig3.h); returns [N,Cout,H,W]."""
     pth = _enum(PATHS, path, "path")
-    if x.dim() != 4:
-        raise ValueError("x must be [N,C,H,W]")
+    if x.dim() != 4 or w_dw.dim() != 4:
+        raise ValueError("x must be [N,C,H,W] and w_dw [C,1,K,K]")
     N, C, H, W = x.shape
+    K = int(w_dw.shape[-1])
     Cout = w_pw.shape[0]
     xp = _dev_f32(x, "x")
-    dp = _dev_f32(w_dw, "w_dw", (C, 1, 3, 3))
+    dp = _dev_f32(w_dw, "w_dw", (C, 1, K, K))
     pp = _dev_f32(w_pw, "w_pw", (Cout, C, 1, 1))
     bp = None if b is None else _dev_f32(b, "b", (Cout,))
     if out is None:
         out = torch.empty((N, Cout, H, W), dtype=torch.float32, device=x.device)
     yp = _dev_f32(out, "out", (N, Cout, H, W))
     with torch.cuda.device(x.device):
-        st = lib.dwsep_conv2d(xp, N, C, H, W, dp, pp, Cout, bp, yp, pth, _stream_handle(stream, x.device))
+        if K == 3:
+            st = lib.dwsep_conv2d(xp, N, C, H, W, dp, pp, Cout, bp, yp, pth, _stream_handle(stream, x.device))
+        else:
+            st = lib.dwsep_conv2d_ex(xp, N, C, H, W, K, dp, pp, Cout, bp, yp, pth, _stream_handle(stream, x.device))
     _check(st)
     return out
 

@@ -40,13 +40,7 @@ struct Halo {
                 "float4 weight rows must stay 16-byte aligned");
 };
 
-// 4-byte asynchronous global -> shared copy; an invalid source (outside the tensor:
-// the zero border) copies nothing and zero-fills the destination.
-__device__ __forceinline__ void cp_async4(float* dst, const float* src, bool valid) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(ig3::smem_addr(dst)), "l"(src),
-               "r"(valid ? 4 : 0)
-               : "memory");
-}
+using ig3::cp_async4;
 
 template <int S, int EPI>
 __global__ void __launch_bounds__(kThreads) conv3d_strided_fma_kernel(
@@ -88,7 +82,7 @@ __global__ void __launch_bounds__(kThreads) conv3d_strided_fma_kernel(
       const bool ok = co < Cout;
       cp_async4(s_w + i, ok ? w + ((size_t)co * Cin + c) * 27 + tap : w, ok);
     }
-    asm volatile("cp.async.commit_group;" ::: "memory");
+    ig3::cp_async_commit();
   };
 
   float acc[2][kTCO];

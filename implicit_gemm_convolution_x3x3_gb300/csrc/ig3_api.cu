@@ -252,6 +252,25 @@ int dwsep_conv2d(const float* x, int N, int C, int H, int W, const float* w_dw, 
   return p == IG3_PATH_TC ? dwsep_tc_launch(a) : dwsep_fma_launch(a);
 }
 
+int dwsep_conv2d_ex(const float* x, int N, int C, int H, int W, int K, const float* w_dw, const float* w_pw, int Cout,
+                    const float* b, float* y, int path, void* stream) {
+  if (K == 3) return dwsep_conv2d(x, N, C, H, W, w_dw, w_pw, Cout, b, y, path, stream);
+  if (K != 1 && K != 5 && K != 7)
+    return fail(IG3_ERR_UNSUPPORTED, "dwsep_conv2d_ex: depthwise size %d (1, 3, 5 or 7 are supported)", K);
+  if (path == IG3_PATH_TC)
+    return fail(IG3_ERR_UNSUPPORTED, "dwsep_conv2d_ex: depthwise size %d runs on the FMA path only", K);
+  // The shape, path and element-count checks of the 3x3 entry point, on the FMA path.
+  const int p = dwsep_select(N, C, H, W, Cout, path == IG3_PATH_AUTO ? IG3_PATH_FMA : path);
+  if (p < 0) return p;
+  if ((long long)C * K * K >= (1ll << 31)) return fail(IG3_ERR_INVALID_ARG, "dwsep_conv2d_ex: w_dw too large");
+  if (!x || !w_dw || !w_pw || !y)
+    return fail(IG3_ERR_INVALID_ARG, "dwsep_conv2d_ex: x, w_dw, w_pw and y must not be NULL");
+  if (!current_device()) return fail(IG3_ERR_CUDA, "dwsep_conv2d_ex: device set-up failed");
+  DwsepArgs a{x, N, C, H, W, w_dw, w_pw, Cout, b, y, static_cast<cudaStream_t>(stream)};
+  a.K = K;
+  return dwsep_fma_launch(a);
+}
+
 const char* ig3_status_string(int status) {
   switch (status) {
     case IG3_OK: return "IG3_OK";

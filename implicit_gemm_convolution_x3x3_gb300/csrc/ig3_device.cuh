@@ -81,6 +81,18 @@ static __device__ __noinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t pa
   }
 }
 
+// ------------------------------------------------------------------ cp.async (4-byte)
+// Asynchronous global -> shared copy of one float; an invalid source (outside the
+// tensor: a zero border) copies nothing and zero-fills the destination.  `src` must
+// still be a valid address.  Complete with cp_async_wait_all() and a barrier.
+__device__ __forceinline__ void cp_async4(float* dst_smem, const float* src, bool valid) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_addr(dst_smem)), "l"(src),
+               "r"(valid ? 4 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // ------------------------------------------------------------------ bulk copies (TMA, 1-D)
 // Global -> this CTA's shared memory, completion counted in bytes on `bar`.
 // src, dst and bytes must all be multiples of 16.

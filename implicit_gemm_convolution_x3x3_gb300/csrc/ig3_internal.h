@@ -39,6 +39,7 @@ struct DwsepArgs {
   const float* b;
   float* y;
   cudaStream_t stream;
+  int K = 3;  // depthwise size (the FMA path also takes 1, 5, 7)
 };
 
 // Records a message for ig3_last_error() (thread-local) and returns `status`.

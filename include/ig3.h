@@ -198,6 +198,20 @@ int dwsep_conv2d(const float* x, int N, int C, int H, int W,
                  const float* w_dw, const float* w_pw, int Cout, const float* b,
                  float* y, int path, void* stream);
 
+/*
+ * dwsep_conv2d with a K x K depthwise stage, K in {1, 3, 5, 7} ([P86], the discussion of
+ * kernel sizes other than 3: a kernel templated on K, dispatched for the common sizes),
+ * stride 1, dilation 1 and "same" padding P = (K-1)/2 (K = 3: P = 1, dwsep_conv2d itself):
+ *   dw[n,c,h,w] = sum_{kh,kw<K} w_dw[c,0,kh,kw] * x[n,c,h+kh-P,w+kw-P]   (zero outside)
+ *   y[n,o,h,w]  = sum_c w_pw[o,c,0,0] * dw[n,c,h,w] + (b ? b[o] : 0)
+ *   w_dw [C][1][K][K]; other arguments as dwsep_conv2d.
+ * K = 3 takes every path of dwsep_conv2d; K = 1, 5, 7 run on the FP32-FMA path
+ * (IG3_PATH_TC returns IG3_ERR_UNSUPPORTED); other K return IG3_ERR_UNSUPPORTED.
+ */
+int dwsep_conv2d_ex(const float* x, int N, int C, int H, int W, int K,
+                    const float* w_dw, const float* w_pw, int Cout, const float* b,
+                    float* y, int path, void* stream);
+
 /* Which path conv3d_fused / dwsep_conv2d would take for these arguments (IG3_PATH_TC or
  * IG3_PATH_FMA), or a negative status if they would be rejected. */
 int conv3d_fused_select_path(int N, int Cin, int D, int H, int W, int Cout, int epilogue, int path);

@@ -148,7 +148,7 @@ class Workload:
             return dict(N=n, Cin=cin, D=d, H=h, W=w, Cout=cout)
         n, c, h, w = self.spec("x").shape
         cout = self.spec("w_pw").shape[0]
-        return dict(N=n, C=c, H=h, W=w, Cout=cout)
+        return dict(N=n, C=c, H=h, W=w, Cout=cout, K=self.spec("w_dw").shape[-1])
 
 
 def _u(a: float) -> tuple:
@@ -171,10 +171,10 @@ def conv3d_workload(name, N, Cin, D, H, W, Cout, seed, epilogue="tanh_mish",
     return Workload(name=name, op="conv3d", seed=seed, tensors=ts, epilogue=epilogue, pad=pad, stride=stride)
 
 
-def dwsep_workload(name, N, C, H, W, Cout, seed, x_dist=NORMAL, with_bias=False) -> Workload:
-    """Depthwise 3x3 (pad 1) then pointwise 1x1: w_dw ~ U(+-1/3), w_pw ~ U(+-1/sqrt(C))."""
+def dwsep_workload(name, N, C, H, W, Cout, seed, x_dist=NORMAL, with_bias=False, K=3) -> Workload:
+    """Depthwise KxK ("same" padding) then pointwise 1x1: w_dw ~ U(+-1/K), w_pw ~ U(+-1/sqrt(C))."""
     ts = [TensorSpec("x", (N, C, H, W), x_dist),
-          TensorSpec("w_dw", (C, 1, 3, 3), _u(1.0 / 3.0)),
+          TensorSpec("w_dw", (C, 1, K, K), _u(1.0 / K)),
           TensorSpec("w_pw", (Cout, C, 1, 1), _u(1.0 / math.sqrt(C)))]
     if with_bias:
         ts.append(TensorSpec("b", (Cout,), _u(1.0 / math.sqrt(C))))
@@ -224,7 +224,12 @@ def conv3d_stride2_tanh_mish() -> Workload:
                            seed=7, epilogue="tanh_mish", pad=1, stride=2)
 
 
+def dwsep_k5() -> Workload:
+    """The dwsep input with a 5x5 depthwise stage (padding 2): x[16,64,512,512] -> 128; seed 8."""
+    return dwsep_workload("dwsep_k5_16x64x512x512_c128", 16, 64, 512, 512, 128, seed=8, K=5)
+
+
 def all_workloads() -> list:
     return [tiny_conv3d(), conv3d_tanh_mish(), conv3d_pool_reduce(), dwsep_conv2d(),
             conv3d_sweep(16), conv3d_sweep(64), conv3d_sweep(128), conv3d_same_tanh_mish(),
-            conv3d_stride2_tanh_mish()]
+            conv3d_stride2_tanh_mish(), dwsep_k5()]

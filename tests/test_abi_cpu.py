@@ -211,3 +211,16 @@ def test_conv3d_ex_argument_errors(lib):
     assert f(*args(5, 1, 2, 4, 1, 0, None)) == -1  # NULL x
     assert q(1, 2, 5, 5, 5, 1, 2, 4, 1, 0) == 0   # stride 2 needs no workspace
     assert q(1, 2, 5, 5, 5, 1, 1, 16, 1, 1) == lib.conv3d_fused_pad_workspace_size(1, 2, 5, 5, 5, 1, 16, 1, 1)
+
+
+def test_dwsep_ex_argument_errors(lib):
+    f = lib.dwsep_conv2d_ex
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] + [ctypes.c_int] * 5 + [ctypes.c_void_p] * 2 + [ctypes.c_int] + \
+        [ctypes.c_void_p] * 2 + [ctypes.c_int, ctypes.c_void_p]
+    assert f(FAKE, 1, 4, 5, 5, 4, FAKE, FAKE, 4, None, FAKE, 2, None) == -2   # K = 4
+    assert f(FAKE, 1, 4, 5, 5, 9, FAKE, FAKE, 4, None, FAKE, 2, None) == -2   # K = 9
+    assert f(FAKE, 1, 16, 8, 8, 5, FAKE, FAKE, 16, None, FAKE, 1, None) == -2  # K = 5 on the TC path
+    assert f(FAKE, 0, 4, 5, 5, 5, FAKE, FAKE, 4, None, FAKE, 0, None) == -1   # N = 0
+    assert f(None, 1, 4, 5, 5, 7, FAKE, FAKE, 4, None, FAKE, 0, None) == -1   # NULL x
+    assert f(FAKE, 70000, 64, 512, 512, 5, FAKE, FAKE, 4, None, FAKE, 2, None) == -1  # too many elements

@@ -93,3 +93,45 @@ def test_dwsep_misaligned_input(ig3):
     out = ig3.dwsep_conv2d(x, w_dw, w_pw, None)
     assert ig3.ig3_last_device_status() == 0
     assert_close(out.cpu().numpy(), ref, "misaligned auto")
+
+
+# ---------------------------------------------------------------- K x K depthwise (FMA path)
+# (N, C, H, W, Cout, K): ragged tiles, channel counts off the 8 / 32 blocks, K = 1, 5, 7.
+K_CASES = [
+    (1, 5, 9, 70, 33, 5),
+    (2, 16, 5, 64, 32, 7),
+    (1, 3, 6, 7, 4, 1),
+    (1, 8, 2, 3, 8, 7),        # image smaller than the kernel
+]
+
+
+@pytest.mark.parametrize("case", K_CASES, ids=lambda s: "x".join(map(str, s)))
+def test_dwsep_k_all_outputs(ig3, case):
+    N, C, H, W, Cout, K = case
+    wl = si.dwsep_workload("t", N, C, H, W, Cout, seed=3300 + sum(case), with_bias=True, K=K)
+    t = wl.generate_all()
+    ref = oracle.dwsep_k(t["x"], t["w_dw"], t["w_pw"], t["b"])
+    for path in ("auto", "fma"):
+        got = ig3.dwsep_conv2d(to_dev(t["x"]), to_dev(t["w_dw"]), to_dev(t["w_pw"]), to_dev(t["b"]), path=path)
+        assert ig3.ig3_last_device_status() == 0
+        assert_close(got.cpu().numpy(), ref, f"{case} {path}")
+    with pytest.raises(ig3.Ig3Error):
+        ig3.dwsep_conv2d(to_dev(t["x"]), to_dev(t["w_dw"]), to_dev(t["w_pw"]), None, path="tc")
+
+
+def test_dwsep_k5_full_size_sampled(ig3):
+    wl = si.dwsep_k5()
+    t = wl.generate_all()
+    x = to_dev(t["x"]); w_dw = to_dev(t["w_dw"]); w_pw = to_dev(t["w_pw"])
+    out = ig3.dwsep_conv2d(x, w_dw, w_pw, None)          # the benchmark's call
+    assert ig3.ig3_last_device_status() == 0
+    idx = sample_indices(tuple(out.shape), 4000, seed=81)
+    rng = np.random.default_rng(82)
+    edges = np.stack([rng.integers(0, 16, 400), rng.integers(0, 128, 400),
+                      rng.choice([0, 1, 510, 511], 400), rng.choice([0, 1, 510, 511], 400)], 1)
+    idx = np.concatenate([idx, edges])
+    got = out[tuple(torch.from_numpy(idx.T).to(out.device))].cpu().numpy()
+    ref = oracle.dwsep_k_at(t["x"], t["w_dw"], t["w_pw"], None, idx)
+    assert_close(got, ref, "dwsep K=5 full sampled")
+    del x, w_dw, w_pw, out
+    torch.cuda.empty_cache()

@@ -67,5 +67,5 @@ def test_every_workload_is_well_formed(wl):
         assert wl.spec("w").shape == (d["Cout"], d["Cin"], 3, 3, 3)
     else:
         d = wl.dims
-        assert wl.spec("w_dw").shape == (d["C"], 1, 3, 3)
+        assert wl.spec("w_dw").shape == (d["C"], 1, d["K"], d["K"]) and d["K"] in (1, 3, 5, 7)
         assert wl.spec("w_pw").shape == (d["Cout"], d["C"], 1, 1)
