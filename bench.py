@@ -396,10 +396,10 @@ def oracle_sample(wl, target_s: float):
     if wl.op == "conv3d":
         _, oh, ow = conv_out_dims(wl)
 
-        def make(planes):
+        def make(planes, items=1):
             # input planes that the first `planes` output planes read (the slab's far
             # end then reads the zero border: the same work, for timing)
-            xs = np.ascontiguousarray(t["x"][0:1, :, 0:max(1, (planes - 1) * wl.stride + 3 - 2 * wl.pad)])
+            xs = np.ascontiguousarray(t["x"][0:items, :, 0:max(1, (planes - 1) * wl.stride + 3 - 2 * wl.pad)])
 
             def run():
                 t0 = time.perf_counter()
@@ -409,27 +409,36 @@ def oracle_sample(wl, target_s: float):
                 elif wl.epilogue == "pool_reduce":
                     oracle.pool_reduce(y, wl.divisor, wl.pool, t["bias2"])
                 return time.perf_counter() - t0
-            return run, 2.0 * d["Cout"] * planes * oh * ow * d["Cin"] * 27
+            return run, 2.0 * items * d["Cout"] * planes * oh * ow * d["Cin"] * 27
         one, _ = make(2)
         dt = one()
         od = conv_out_dims(wl)[0]
         planes = int(max(2, min(od, 2 * target_s / max(dt, 1e-3))))
-        run, fl = make(planes)
-        return run, fl, f"batch item 0, {planes} of {od} output planes, all {d['Cout']} channels"
+        if planes < od:
+            run, fl = make(planes)
+            return run, fl, f"batch item 0, {planes} of {od} output planes, all {d['Cout']} channels"
+        # a whole batch item fits the budget: take as many items as it allows
+        items = int(max(1, min(d["N"], target_s / max(dt * od / 2, 1e-3))))
+        run, fl = make(od, items)
+        return run, fl, f"batch items 0..{items - 1} of {d['N']}, all {od} output planes, all {d['Cout']} channels"
 
-    def make(rows):
-        xs = np.ascontiguousarray(t["x"][0:1, :, 0:rows])
+    def make(rows, items=1):
+        xs = np.ascontiguousarray(t["x"][0:items, :, 0:rows])
 
         def run():
             t0 = time.perf_counter()
             oracle.dwsep_k(xs, t["w_dw"], t["w_pw"], t.get("b"))
             return time.perf_counter() - t0
-        return run, 2.0 * rows * d["W"] * d["C"] * (d["K"] * d["K"] + d["Cout"])
+        return run, 2.0 * items * rows * d["W"] * d["C"] * (d["K"] * d["K"] + d["Cout"])
     one, _ = make(8)
     dt = one()
     rows = int(max(8, min(d["H"], 8 * target_s / max(dt, 1e-3))))
-    run, fl = make(rows)
-    return run, fl, f"batch item 0, first {rows} of {d['H']} rows, all {d['Cout']} channels"
+    if rows < d["H"]:
+        run, fl = make(rows)
+        return run, fl, f"batch item 0, first {rows} of {d['H']} rows, all {d['Cout']} channels"
+    items = int(max(1, min(d["N"], target_s / max(dt * d["H"] / 8, 1e-3))))
+    run, fl = make(d["H"], items)
+    return run, fl, f"batch items 0..{items - 1} of {d['N']}, all {d['H']} rows, all {d['Cout']} channels"
 
 
 def cpu_baseline_sample(wl, target_s: float) -> dict:
