@@ -99,6 +99,119 @@ __global__ void __launch_bounds__(kThreads) dwsep_fma_kernel(const float* __rest
   }
 }
 
+// Two-phase form for the larger depthwise sizes (K = 5, 7), where recomputing the K*K
+// depthwise sum for every group of output channels and reading it tap by tap from
+// shared memory would cost more than the pointwise work: per channel chunk the CTA
+// first forms the depthwise values of its 64 x 4 pixels once (a thread: 4 adjacent
+// pixels of one row for 2 channels, the input row read as float4 and slid across the
+// K taps) into shared memory, then each thread takes one pixel for 64 output channels
+// (one depthwise read and sixteen broadcast float4 weight reads per channel for 64 FMAs).
+constexpr int k2CO = 64;
+
+template <int K>
+__global__ void __launch_bounds__(kThreads) dwsep_fma2_kernel(const float* __restrict__ x,
+                                                              const float* __restrict__ w_dw,
+                                                              const float* __restrict__ w_pw,
+                                                              const float* __restrict__ bias, float* __restrict__ y,
+                                                              int N, int C, int H, int W, int Cout) {
+  constexpr int P = (K - 1) / 2;
+  constexpr int kXW = kTW + K - 1, kXWPad = (kXW + 3) / 4 * 4 + ((K + 3 + 3) / 4 * 4 > K + 3 ? 4 : 0);
+  constexpr int kXH = kTH + K - 1;
+  constexpr int kRowV = (K + 3 + 3) / 4;  // float4 reads per input row (covers 4 pixels + K - 1)
+  static_assert(4 * (kTW / 4 - 1) + 4 * kRowV <= kXWPad, "row reads stay inside the padded halo row");
+  __shared__ __align__(16) float s_x[kCC][kXH][kXWPad];
+  __shared__ float s_dw[kCC][K * K];
+  __shared__ float s_d[kCC][kTH][kTW];
+  __shared__ __align__(16) float s_pw[kCC][k2CO];
+
+  const int tiles_w = (W + kTW - 1) / kTW;
+  const int w0 = (blockIdx.x % tiles_w) * kTW;
+  const int h0 = (blockIdx.x / tiles_w) * kTH;
+  const int cgroups = (Cout + k2CO - 1) / k2CO;
+  const int n = blockIdx.y / cgroups;
+  const int co0 = (blockIdx.y % cgroups) * k2CO;
+  const int tid = threadIdx.x;
+  const int px = tid % kTW, py = tid / kTW;                               // phase 2
+  const int g = tid % 16, r1 = (tid / 16) % kTH, cp = tid / (16 * kTH);   // phase 1
+
+  float acc[k2CO];
+#pragma unroll
+  for (int j = 0; j < k2CO; ++j) acc[j] = 0.0f;
+
+  const size_t plane = (size_t)H * W;
+  for (int c0 = 0; c0 < C; c0 += kCC) {
+    __syncthreads();
+    for (int row = tid / 32; row < kCC * kXH; row += kThreads / 32) {
+      const int c = row / kXH, yy = row % kXH;
+      const int gc = c0 + c, gh = h0 + yy - P;
+      const bool row_in = gc < C && gh >= 0 && gh < H;
+      const float* src = row_in ? x + ((size_t)n * C + gc) * plane + (size_t)gh * W : x;
+      for (int xx = tid % 32; xx < kXW; xx += 32) {
+        const int gw = w0 + xx - P;
+        const bool ok = row_in && gw >= 0 && gw < W;
+        cp_async4(&s_x[c][yy][xx], ok ? src + gw : x, ok);
+      }
+    }
+    for (int i = tid; i < kCC * K * K; i += kThreads) {
+      const int c = i / (K * K), t = i % (K * K);
+      const bool ok = c0 + c < C;
+      cp_async4(&s_dw[c][t], ok ? &w_dw[(size_t)(c0 + c) * (K * K) + t] : w_dw, ok);
+    }
+    for (int i = tid; i < kCC * k2CO; i += kThreads) {
+      const int c = i / k2CO, co = i % k2CO;
+      const bool ok = c0 + c < C && co0 + co < Cout;
+      cp_async4(&s_pw[c][co], ok ? &w_pw[(size_t)(co0 + co) * C + c0 + c] : w_pw, ok);
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    // Phase 1: depthwise values of 4 adjacent pixels, channels 2cp and 2cp + 1.
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      const int c = 2 * cp + cc;
+      float dv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int kh = 0; kh < K; ++kh) {
+        float row[4 * kRowV];
+#pragma unroll
+        for (int v = 0; v < kRowV; ++v) {
+          const float4 q = *reinterpret_cast<const float4*>(&s_x[c][r1 + kh][4 * g + 4 * v]);
+          row[4 * v] = q.x; row[4 * v + 1] = q.y; row[4 * v + 2] = q.z; row[4 * v + 3] = q.w;
+        }
+#pragma unroll
+        for (int kw = 0; kw < K; ++kw) {
+          const float wv = s_dw[c][kh * K + kw];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) dv[j] = fmaf(row[j + kw], wv, dv[j]);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) s_d[c][r1][4 * g + j] = dv[j];
+    }
+    __syncthreads();
+    // Phase 2: the pointwise products of this thread's pixel.
+#pragma unroll 2
+    for (int c = 0; c < kCC; ++c) {
+      const float d = s_d[c][py][px];
+#pragma unroll
+      for (int j = 0; j < k2CO; j += 4) {
+        const float4 p = *reinterpret_cast<const float4*>(&s_pw[c][j]);
+        acc[j] = fmaf(d, p.x, acc[j]);
+        acc[j + 1] = fmaf(d, p.y, acc[j + 1]);
+        acc[j + 2] = fmaf(d, p.z, acc[j + 2]);
+        acc[j + 3] = fmaf(d, p.w, acc[j + 3]);
+      }
+    }
+  }
+
+  const int h = h0 + py, w = w0 + px;
+  if (h >= H || w >= W) return;
+#pragma unroll
+  for (int j = 0; j < k2CO; ++j) {
+    const int co = co0 + j;
+    if (co < Cout) y[((size_t)n * Cout + co) * plane + (size_t)h * W + w] = acc[j] + (bias ? __ldg(&bias[co]) : 0.0f);
+  }
+}
+
 }  // namespace
 
 int dwsep_fma_launch(const DwsepArgs& a) {
@@ -106,11 +219,13 @@ int dwsep_fma_launch(const DwsepArgs& a) {
   const long long zy = (long long)a.N * ((a.Cout + kCO - 1) / kCO);
   if (tiles > 0x7fffffffLL || zy > 65535) return fail(IG3_ERR_UNSUPPORTED, "dwsep FMA path: grid too large");
   const dim3 grid((unsigned)tiles, (unsigned)zy);
+  const long long zy2 = (long long)a.N * ((a.Cout + k2CO - 1) / k2CO);
+  const dim3 grid2((unsigned)tiles, (unsigned)zy2);
   switch (a.K) {
     case 1: dwsep_fma_kernel<1><<<grid, kThreads, 0, a.stream>>>(a.x, a.w_dw, a.w_pw, a.b, a.y, a.N, a.C, a.H, a.W, a.Cout); break;
     case 3: dwsep_fma_kernel<3><<<grid, kThreads, 0, a.stream>>>(a.x, a.w_dw, a.w_pw, a.b, a.y, a.N, a.C, a.H, a.W, a.Cout); break;
-    case 5: dwsep_fma_kernel<5><<<grid, kThreads, 0, a.stream>>>(a.x, a.w_dw, a.w_pw, a.b, a.y, a.N, a.C, a.H, a.W, a.Cout); break;
-    case 7: dwsep_fma_kernel<7><<<grid, kThreads, 0, a.stream>>>(a.x, a.w_dw, a.w_pw, a.b, a.y, a.N, a.C, a.H, a.W, a.Cout); break;
+    case 5: dwsep_fma2_kernel<5><<<grid2, kThreads, 0, a.stream>>>(a.x, a.w_dw, a.w_pw, a.b, a.y, a.N, a.C, a.H, a.W, a.Cout); break;
+    case 7: dwsep_fma2_kernel<7><<<grid2, kThreads, 0, a.stream>>>(a.x, a.w_dw, a.w_pw, a.b, a.y, a.N, a.C, a.H, a.W, a.Cout); break;
     default: return fail(IG3_ERR_UNSUPPORTED, "dwsep FMA path: depthwise size %d (1, 3, 5 or 7)", a.K);
   }
   return count_launch(cuda_status(cudaGetLastError(), "dwsep FMA kernel launch"));
