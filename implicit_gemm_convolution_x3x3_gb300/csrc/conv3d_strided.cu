@@ -9,25 +9,27 @@
 //
 // Stride 2 breaks the tensor-core kernel's addressing (the tap shift is a descriptor
 // offset into one tile of consecutive positions; strided positions are not), so it
-// runs on the FMA pipe: a CTA computes 16 x 32 outputs of one plane for 16 output
-// channels, two rows per thread (32 accumulators).  Each input channel's strided halo,
-// 3 x ((16-1)S+3) x ((32-1)S+3), and its weights for the 16 outputs are staged in
+// runs on the FMA pipe: a CTA computes 16 x 32 outputs of one plane for 32 output
+// channels, two rows per thread (64 accumulators).  Each input channel's strided halo,
+// 3 x ((16-1)S+3) x ((32-1)S+3), and its weights for the 32 outputs are staged in
 // shared memory by 4-byte cp.async copies whose zero-fill is the padding, two stages
-// deep: the next channel's copies fly while this one is computed.  Per tap a thread reads two input values and
-// four float4 weight rows (the same for the whole CTA: broadcasts) and does 32 FMAs.
+// deep: the next channel's copies fly while this one is computed.  The kernel is
+// bound by instruction issue, so each staged input feeds as many FMAs as the
+// registers allow (32 output channels: per tap two input reads and eight broadcast
+// float4 weight rows, the same for the whole CTA, for 64 FMAs).
 #include <cstdint>
 
 #include "ig3_internal.h"
 
 namespace {
 
-// CTA: 16 x 32 outputs of one plane x 16 output channels; thread (ty, tx) takes rows
-// ty and ty + 8 of column tx (32 accumulators).
-constexpr int kTH = 16, kTW = 32, kTCO = 16, kThreads = 256;
+// CTA: 16 x 32 outputs of one plane x 32 output channels; thread (ty, tx) takes rows
+// ty and ty + 8 of column tx (64 accumulators).
+constexpr int kTH = 16, kTW = 32, kTCO = 32, kThreads = 256;
 constexpr int kMaxPad = 16;
 
 // One stage = one input channel: its 3 x H x W strided halo, then its weights for the
-// CTA's 16 output channels.  Two stages: the copies of channel c+1 fly while channel c
+// CTA's 32 output channels.  Two stages: the copies of channel c+1 fly while channel c
 // is computed.
 template <int S>
 struct Halo {
