@@ -5,6 +5,7 @@ rank's, and its throughput counts every rank's work.  The only collectives are t
 timing barrier and that max.  These tests run two gloo ranks on the CPU; the GPU
 kernels play no part.
 """
+import json
 import os
 import socket
 import subprocess
@@ -83,3 +84,23 @@ def test_reference_arm_runs_on_rank_zero_only():
                         "--warmup", "3", "--workload", "tiny"], env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr
     assert r.stdout.strip() == ""
+
+
+@pytest.mark.parametrize("workload", ["tiny", "conv3d_s2"])
+def test_reference_arm_json_line(workload):
+    # Rank 0 (or no launcher): one JSON line with the benchmark contract's keys, the
+    # oracle timed on a bounded sample of the workload.
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "3", "--workload", workload], env=env, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stderr
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["value"] > 0 and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
