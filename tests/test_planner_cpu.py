@@ -1,0 +1,32 @@
+"""The tensor-core conv3d planner and its index arithmetic, checked on the host.
+
+tests/planner_check.cu includes the planner (csrc/conv3d_tc.cu) and, for every work
+unit of every CTA, recomputes the indices the kernel uses (TMEM columns, slots, B
+blocks, A rows, shared-memory offsets, input copies) against the plan's buffers.  It
+needs nvcc (host compilation only) but no GPU.
+"""
+import os
+import shutil
+import subprocess
+import tempfile
+
+import pytest
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+
+
+def test_planner_index_bounds():
+    nvcc = shutil.which("nvcc") or ("/usr/local/cuda/bin/nvcc" if os.path.exists("/usr/local/cuda/bin/nvcc") else None)
+    if nvcc is None:
+        pytest.skip("nvcc not available")
+    with tempfile.TemporaryDirectory() as d:
+        exe = os.path.join(d, "planner_check")
+        cmd = [nvcc, "-std=c++17", "-O1", "-gencode", "arch=compute_103a,code=sm_103a",
+               "-I" + os.path.join(ROOT, "include"), "-o", exe, os.path.join(HERE, "planner_check.cu"),
+               "-Xlinker", "--unresolved-symbols=ignore-all"]
+        b = subprocess.run(cmd, capture_output=True, text=True, timeout=600)
+        assert b.returncode == 0, b.stderr[-2000:]
+        r = subprocess.run([exe], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-3000:]
+    assert "fails: 0" in r.stdout
