@@ -106,7 +106,26 @@ __global__ void __launch_bounds__(kThreads) dwsep_fma_kernel(const float* __rest
 // pixels of one row for 2 channels, the input row read as float4 and slid across the
 // K taps) into shared memory, then each thread takes one pixel for 64 output channels
 // (one depthwise read and sixteen broadcast float4 weight reads per channel for 64 FMAs).
+// Two stages of copies: the next chunk's fly while this one is computed.
 constexpr int k2CO = 64;
+
+// Shared-memory layout of the two-phase kernel: two stages (input halo, depthwise
+// weights, pointwise weights of one channel chunk), then the depthwise results.
+template <int K>
+struct Fma2Smem {
+  static constexpr int XW = kTW + K - 1;
+  static constexpr int RowV = (K + 3 + 3) / 4;  // float4 reads per input row (4 pixels + K - 1)
+  static constexpr int XWPad = (XW + 3) / 4 * 4 + (4 * RowV > K + 3 ? 4 : 0);
+  static constexpr int XH = kTH + K - 1;
+  static constexpr int x_floats = kCC * XH * XWPad;
+  static constexpr int dw_floats = (kCC * K * K + 3) / 4 * 4;
+  static constexpr int pw_floats = kCC * k2CO;
+  static constexpr int stage_floats = x_floats + dw_floats + pw_floats;
+  static constexpr int d_floats = kCC * kTH * kTW;
+  static constexpr size_t bytes = (size_t)(2 * stage_floats + d_floats) * sizeof(float);
+  static_assert(x_floats % 4 == 0 && stage_floats % 4 == 0, "float4 reads stay 16-byte aligned");
+  static_assert(4 * (kTW / 4 - 1) + 4 * RowV <= XWPad, "row reads stay inside the padded halo row");
+};
 
 template <int K>
 __global__ void __launch_bounds__(kThreads) dwsep_fma2_kernel(const float* __restrict__ x,
@@ -114,15 +133,10 @@ __global__ void __launch_bounds__(kThreads) dwsep_fma2_kernel(const float* __res
                                                               const float* __restrict__ w_pw,
                                                               const float* __restrict__ bias, float* __restrict__ y,
                                                               int N, int C, int H, int W, int Cout) {
+  using L = Fma2Smem<K>;
   constexpr int P = (K - 1) / 2;
-  constexpr int kXW = kTW + K - 1, kXWPad = (kXW + 3) / 4 * 4 + ((K + 3 + 3) / 4 * 4 > K + 3 ? 4 : 0);
-  constexpr int kXH = kTH + K - 1;
-  constexpr int kRowV = (K + 3 + 3) / 4;  // float4 reads per input row (covers 4 pixels + K - 1)
-  static_assert(4 * (kTW / 4 - 1) + 4 * kRowV <= kXWPad, "row reads stay inside the padded halo row");
-  __shared__ __align__(16) float s_x[kCC][kXH][kXWPad];
-  __shared__ float s_dw[kCC][K * K];
-  __shared__ float s_d[kCC][kTH][kTW];
-  __shared__ __align__(16) float s_pw[kCC][k2CO];
+  extern __shared__ __align__(16) float smem[];
+  float* s_d = smem + 2 * L::stage_floats;  // [kCC][kTH][kTW]
 
   const int tiles_w = (W + kTW - 1) / kTW;
   const int w0 = (blockIdx.x % tiles_w) * kTW;
@@ -133,37 +147,53 @@ __global__ void __launch_bounds__(kThreads) dwsep_fma2_kernel(const float* __res
   const int tid = threadIdx.x;
   const int px = tid % kTW, py = tid / kTW;                               // phase 2
   const int g = tid % 16, r1 = (tid / 16) % kTH, cp = tid / (16 * kTH);   // phase 1
-
-  float acc[k2CO];
-#pragma unroll
-  for (int j = 0; j < k2CO; ++j) acc[j] = 0.0f;
-
   const size_t plane = (size_t)H * W;
-  for (int c0 = 0; c0 < C; c0 += kCC) {
-    __syncthreads();
-    for (int row = tid / 32; row < kCC * kXH; row += kThreads / 32) {
-      const int c = row / kXH, yy = row % kXH;
+
+  // Copies of the chunk starting at channel c0 into stage st (zero-fill = padding).
+  auto stage_in = [&](int c0, int st) {
+    float* s_x = smem + st * L::stage_floats;
+    float* s_dw = s_x + L::x_floats;
+    float* s_pw = s_dw + L::dw_floats;
+    for (int row = tid / 32; row < kCC * L::XH; row += kThreads / 32) {
+      const int c = row / L::XH, yy = row % L::XH;
       const int gc = c0 + c, gh = h0 + yy - P;
       const bool row_in = gc < C && gh >= 0 && gh < H;
       const float* src = row_in ? x + ((size_t)n * C + gc) * plane + (size_t)gh * W : x;
-      for (int xx = tid % 32; xx < kXW; xx += 32) {
+      for (int xx = tid % 32; xx < L::XW; xx += 32) {
         const int gw = w0 + xx - P;
         const bool ok = row_in && gw >= 0 && gw < W;
-        cp_async4(&s_x[c][yy][xx], ok ? src + gw : x, ok);
+        cp_async4(s_x + row * L::XWPad + xx, ok ? src + gw : x, ok);
       }
     }
     for (int i = tid; i < kCC * K * K; i += kThreads) {
       const int c = i / (K * K), t = i % (K * K);
       const bool ok = c0 + c < C;
-      cp_async4(&s_dw[c][t], ok ? &w_dw[(size_t)(c0 + c) * (K * K) + t] : w_dw, ok);
+      cp_async4(s_dw + i, ok ? &w_dw[(size_t)(c0 + c) * (K * K) + t] : w_dw, ok);
     }
     for (int i = tid; i < kCC * k2CO; i += kThreads) {
       const int c = i / k2CO, co = i % k2CO;
       const bool ok = c0 + c < C && co0 + co < Cout;
-      cp_async4(&s_pw[c][co], ok ? &w_pw[(size_t)(co0 + co) * C + c0 + c] : w_pw, ok);
+      cp_async4(s_pw + i, ok ? &w_pw[(size_t)(co0 + co) * C + c0 + c] : w_pw, ok);
     }
-    cp_async_wait_all();
+    cp_async_commit();
+  };
+
+  float acc[k2CO];
+#pragma unroll
+  for (int j = 0; j < k2CO; ++j) acc[j] = 0.0f;
+
+  stage_in(0, 0);
+  for (int c0 = 0, st = 0; c0 < C; c0 += kCC, st ^= 1) {
+    if (c0 + kCC < C) {
+      stage_in(c0 + kCC, st ^ 1);  // that stage was last read before the barrier ending c0 - kCC
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    } else {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+    }
     __syncthreads();
+    const float* s_x = smem + st * L::stage_floats;
+    const float* s_dw = s_x + L::x_floats;
+    const float* s_pw = s_dw + L::dw_floats;
     // Phase 1: depthwise values of 4 adjacent pixels, channels 2cp and 2cp + 1.
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc) {
@@ -171,36 +201,38 @@ __global__ void __launch_bounds__(kThreads) dwsep_fma2_kernel(const float* __res
       float dv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
       for (int kh = 0; kh < K; ++kh) {
-        float row[4 * kRowV];
+        float row[4 * L::RowV];
+        const float* xr = s_x + (c * L::XH + r1 + kh) * L::XWPad + 4 * g;
 #pragma unroll
-        for (int v = 0; v < kRowV; ++v) {
-          const float4 q = *reinterpret_cast<const float4*>(&s_x[c][r1 + kh][4 * g + 4 * v]);
+        for (int v = 0; v < L::RowV; ++v) {
+          const float4 q = *reinterpret_cast<const float4*>(xr + 4 * v);
           row[4 * v] = q.x; row[4 * v + 1] = q.y; row[4 * v + 2] = q.z; row[4 * v + 3] = q.w;
         }
 #pragma unroll
         for (int kw = 0; kw < K; ++kw) {
-          const float wv = s_dw[c][kh * K + kw];
+          const float wv = s_dw[c * K * K + kh * K + kw];
 #pragma unroll
           for (int j = 0; j < 4; ++j) dv[j] = fmaf(row[j + kw], wv, dv[j]);
         }
       }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) s_d[c][r1][4 * g + j] = dv[j];
+      for (int j = 0; j < 4; ++j) s_d[(c * kTH + r1) * kTW + 4 * g + j] = dv[j];
     }
     __syncthreads();
     // Phase 2: the pointwise products of this thread's pixel.
 #pragma unroll 2
     for (int c = 0; c < kCC; ++c) {
-      const float d = s_d[c][py][px];
+      const float d = s_d[(c * kTH + py) * kTW + px];
 #pragma unroll
       for (int j = 0; j < k2CO; j += 4) {
-        const float4 p = *reinterpret_cast<const float4*>(&s_pw[c][j]);
+        const float4 p = *reinterpret_cast<const float4*>(s_pw + c * k2CO + j);
         acc[j] = fmaf(d, p.x, acc[j]);
         acc[j + 1] = fmaf(d, p.y, acc[j + 1]);
         acc[j + 2] = fmaf(d, p.z, acc[j + 2]);
         acc[j + 3] = fmaf(d, p.w, acc[j + 3]);
       }
     }
+    __syncthreads();  // stage st and s_d are rewritten on the next iterations
   }
 
   const int h = h0 + py, w = w0 + px;
@@ -224,8 +256,18 @@ int dwsep_fma_launch(const DwsepArgs& a) {
   switch (a.K) {
     case 1: dwsep_fma_kernel<1><<<grid, kThreads, 0, a.stream>>>(a.x, a.w_dw, a.w_pw, a.b, a.y, a.N, a.C, a.H, a.W, a.Cout); break;
     case 3: dwsep_fma_kernel<3><<<grid, kThreads, 0, a.stream>>>(a.x, a.w_dw, a.w_pw, a.b, a.y, a.N, a.C, a.H, a.W, a.Cout); break;
-    case 5: dwsep_fma2_kernel<5><<<grid2, kThreads, 0, a.stream>>>(a.x, a.w_dw, a.w_pw, a.b, a.y, a.N, a.C, a.H, a.W, a.Cout); break;
-    case 7: dwsep_fma2_kernel<7><<<grid2, kThreads, 0, a.stream>>>(a.x, a.w_dw, a.w_pw, a.b, a.y, a.N, a.C, a.H, a.W, a.Cout); break;
+    case 5:
+    case 7: {
+      auto go = [&](auto kernel, size_t smem) -> int {
+        const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return cuda_status(e, "dwsep FMA path: set shared memory size");
+        kernel<<<grid2, kThreads, smem, a.stream>>>(a.x, a.w_dw, a.w_pw, a.b, a.y, a.N, a.C, a.H, a.W, a.Cout);
+        return IG3_OK;
+      };
+      const int st = a.K == 5 ? go(dwsep_fma2_kernel<5>, Fma2Smem<5>::bytes) : go(dwsep_fma2_kernel<7>, Fma2Smem<7>::bytes);
+      if (st != IG3_OK) return st;
+      break;
+    }
     default: return fail(IG3_ERR_UNSUPPORTED, "dwsep FMA path: depthwise size %d (1, 3, 5 or 7)", a.K);
   }
   return count_launch(cuda_status(cudaGetLastError(), "dwsep FMA kernel launch"));
