@@ -1,9 +1,11 @@
-"""The tensor-core conv3d planner and its index arithmetic, checked on the host.
+"""The tensor-core planners and the addresses their kernels derive, checked on the host.
 
-tests/planner_check.cu includes the planner (csrc/conv3d_tc.cu) and, for every work
-unit of every CTA, recomputes the indices the kernel uses (TMEM columns, slots, B
-blocks, A rows, shared-memory offsets, input copies) against the plan's buffers.  It
-needs nvcc (host compilation only) but no GPU.
+tests/planner_check.cu includes the conv3d planner (csrc/conv3d_tc.cu) and, for every
+work unit of every CTA, recomputes the indices the kernel uses (TMEM columns, slots, B
+blocks, A rows, shared-memory offsets, input copies) against the plan's buffers;
+tests/dwsep_plan_check.cu does the same for the depthwise-separable planner (strips,
+shared-memory layout, TMEM ranges, tensor-map box and strides, row-copy coordinates).
+They need nvcc (host compilation only) but no GPU.
 """
 import os
 import shutil
@@ -16,14 +18,15 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 
 
-def test_planner_index_bounds():
+@pytest.mark.parametrize("checker", ["planner_check.cu", "dwsep_plan_check.cu"])
+def test_planner_index_bounds(checker):
     nvcc = shutil.which("nvcc") or ("/usr/local/cuda/bin/nvcc" if os.path.exists("/usr/local/cuda/bin/nvcc") else None)
     if nvcc is None:
         pytest.skip("nvcc not available")
     with tempfile.TemporaryDirectory() as d:
-        exe = os.path.join(d, "planner_check")
+        exe = os.path.join(d, checker[:-3])
         cmd = [nvcc, "-std=c++17", "-O1", "-gencode", "arch=compute_103a,code=sm_103a",
-               "-I" + os.path.join(ROOT, "include"), "-o", exe, os.path.join(HERE, "planner_check.cu"),
+               "-I" + os.path.join(ROOT, "include"), "-o", exe, os.path.join(HERE, checker),
                "-Xlinker", "--unresolved-symbols=ignore-all"]
         b = subprocess.run(cmd, capture_output=True, text=True, timeout=600)
         assert b.returncode == 0, b.stderr[-2000:]
