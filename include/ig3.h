@@ -1,5 +1,8 @@
 /*
- * ig3 -- fused stride-1 3x3(x3) convolutions for NVIDIA GB300 (sm_103a).
+ * ig3 -- fused 3x3(x3) convolutions for NVIDIA GB300 (sm_103a): stride-1 valid conv3d
+ * and depthwise 3x3 -> pointwise 1x1 conv2d with fused epilogues, plus zero-padded and
+ * stride-2 conv3d (conv3d_fused_pad, conv3d_fused_ex) and K x K depthwise stages
+ * (dwsep_conv2d_ex).
  *
  * A plain C ABI: raw pointers, sizes and a CUDA stream passed as `void*`
  * (a cudaStream_t; NULL = the legacy default stream).  No C++ or framework
