@@ -361,10 +361,13 @@ const char* conv3d_tc_unsupported_reason(int N, int Cin, int D, int H, int W, in
 
 size_t conv3d_tc_workspace(const Conv3dArgs& a) {
   Plan pl = make_plan(a.N, a.Cin, a.D, a.H, a.W, a.Cout, a.epi, 148);
-  return pl.ok ? pl.blob_bytes + pl.partial_bytes : 0;
+  const size_t own = pl.ok ? pl.blob_bytes + pl.partial_bytes : 0;
+  // Either kernel may run (the A-in-tensor-memory one needs x 16-byte aligned).
+  return conv3d_tc16_applies(a, nullptr) ? std::max(own, conv3d_tc16_workspace(a)) : own;
 }
 
 int conv3d_tc_launch(const Conv3dArgs& a) {
+  if (reinterpret_cast<uintptr_t>(a.x) % 16 == 0 && conv3d_tc16_applies(a, nullptr)) return conv3d_tc16_launch(a);
   const int sms = num_sms();
   if (sms <= 0) return fail(IG3_ERR_CUDA, "conv3d TC path: cannot query the SM count");
   Plan pl = make_plan(a.N, a.Cin, a.D, a.H, a.W, a.Cout, a.epi, sms);

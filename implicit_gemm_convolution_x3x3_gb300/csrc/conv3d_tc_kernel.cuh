@@ -92,12 +92,6 @@ static __host__ __device__ __forceinline__ uint32_t slot_add(const TcParams& p, 
   return (s0 + (uint32_t)k) % (uint32_t)p.NSLOT;
 }
 
-// A bounded wait used while shutting down: ignores the abort flag.
-static __device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity, const WaitCtl& ctl) {
-  int never = 0;
-  return mbar_wait_bounded(bar, parity, ctl, &never);
-}
-
 // A bounded wait taken by every lane of a warp, returning one verdict for the whole
 // warp (and leaving it converged): warp-collective tcgen05 instructions follow.
 static __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& ctl, volatile int* abort) {

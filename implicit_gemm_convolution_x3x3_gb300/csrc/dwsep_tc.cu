@@ -232,8 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       umma_commit(mma_done);
-      int never = 0;
-      mbar_wait_bounded(mma_done, 0, p.ctl, &never);
+      drain_wait(mma_done, 0, p.ctl);
     }
   } else if (warp == kLoadWarp) {
     // ------------------------------------------------------------ row loader
@@ -265,8 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             --back.idx;
           }
-          int never = 0;
-          mbar_wait_bounded(&row_full[back.idx], back.phase, p.ctl, &never);
+          drain_wait(&row_full[back.idx], back.phase, p.ctl);
         }
       }
     }
@@ -464,22 +462,6 @@ DwPlan make_dw_plan(int N, int C, int H, int W, int Cout, int sms = 148) {
   pl.smem = std::max(pl.smem, (size_t)(116 * 1024));  // one CTA (one TMEM owner) per SM
   pl.ok = true;
   return pl;
-}
-
-// The driver's tensor-map encoder, looked up once through the runtime (no link-time
-// dependency on the driver library).
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static std::once_flag once;
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  });
-  return fn;
 }
 
 }  // namespace

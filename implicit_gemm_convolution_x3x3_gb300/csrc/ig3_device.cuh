@@ -81,6 +81,20 @@ static __device__ __noinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t pa
   }
 }
 
+// A bounded wait taken while shutting down, for copies or MMAs this CTA already
+// issued: it ignores the abort flag, and its limit is at least kDrainFloorNs
+// whatever limit the caller set for the ordinary waits.  Issued bulk copies and
+// MMAs always complete, so a short user limit must not let a drain give up while
+// they are still in flight (the CTA would exit, or free tensor memory, under them).
+constexpr unsigned long long kDrainFloorNs = 1000000000ull;  // 1 s
+
+static __device__ __noinline__ bool drain_wait(uint64_t* bar, uint32_t parity, const WaitCtl& ctl) {
+  WaitCtl c = ctl;
+  if (c.limit_ns < kDrainFloorNs) c.limit_ns = kDrainFloorNs;
+  int never = 0;
+  return mbar_wait_bounded(bar, parity, c, &never);
+}
+
 // ------------------------------------------------------------------ cp.async (4-byte)
 // Asynchronous global -> shared copy of one float; an invalid source (outside the
 // tensor: a zero border) copies nothing and zero-fills the destination.  `src` must

@@ -4,7 +4,9 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include "ig3.h"
 #include "ig3_device.cuh"
@@ -53,6 +55,9 @@ int count_launch(int status);
 WaitCtl wait_ctl();
 // Number of SMs of the current device (cached).
 int num_sms();
+// The driver's tensor-map encoder, looked up once through the runtime (no link-time
+// dependency on the driver library); nullptr if unavailable.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -68,6 +73,12 @@ int conv3d_fma_launch(const Conv3dArgs& a);
 const char* conv3d_tc_unsupported_reason(int N, int Cin, int D, int H, int W, int Cout, int epi);
 size_t conv3d_tc_workspace(const Conv3dArgs& a);
 int conv3d_tc_launch(const Conv3dArgs& a);
+
+// ---- tensor-core path for 16 output channels with A in tensor memory (conv3d_tc16.cu);
+// conv3d_tc_launch takes it wherever it applies and x is 16-byte aligned.
+bool conv3d_tc16_applies(const Conv3dArgs& a, const char** why);
+size_t conv3d_tc16_workspace(const Conv3dArgs& a);
+int conv3d_tc16_launch(const Conv3dArgs& a);
 
 // ---- depthwise-separable (dwsep.cu)
 const char* dwsep_tc_unsupported_reason(int N, int C, int H, int W, int Cout);

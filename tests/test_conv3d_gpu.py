@@ -70,6 +70,13 @@ SMALL_CASES = [
     (1, 40, 5, 6, 64, 16),    #   five K-steps of resident weights
     (1, 136, 5, 6, 64, 16),   #   streamed weights
     (1, 8, 5, 9, 20, 16),     # Cout = 16 with W not dividing 128: hi and lo columns instead
+    (1, 12, 9, 7, 64, 16),    # Cout = 16, A in tensor memory: a half-empty second K-step
+    (2, 3, 7, 5, 32, 16),     #   three input channels
+    (1, 24, 12, 6, 16, 16),   #   three channel chunks per plane
+    (3, 8, 20, 10, 64, 16),   #   many planes per unit: the slot ring wraps inside units
+    (1, 32, 12, 6, 128, 16),  #   two chunks of two K-steps, W = 128
+    (2, 16, 6, 5, 12, 16),    #   H*W % 4 == 0 but W not dividing 128: the other kernel
+    (1, 8, 5, 7, 6, 16),      #   H*W % 4 != 0: the other kernel
     (2, 3, 5, 7, 9, 5),       # odd channel counts
     (1, 1, 3, 3, 3, 1),       # smallest valid input: one output
 ]
@@ -155,6 +162,10 @@ POOL_CASES = [
     (2, 8, 6, 10, 32, 16),    # W = 32
     (1, 8, 6, 12, 4, 16),     # W = 4
     (2, 8, 8, 64, 64, 16),    # two position tiles per unit
+    (2, 3, 7, 5, 32, 16),     # odd conv-output depth, three input channels
+    (4, 8, 33, 10, 64, 16),   # 31 conv-output planes: several plane splits
+    (1, 12, 9, 7, 16, 16),    # a half-empty second K-step, odd depth
+    (3, 24, 6, 6, 8, 16),     # three channel chunks
 ]
 
 
@@ -184,6 +195,21 @@ def test_pool_reduce_full_size_sampled_and_deterministic(ig3):
     for n in (0, 1, 64, 127):
         ref = oracle.conv3d_pool_reduce(t["x"][n:n + 1], t["w"], t["b"], 2.0, 2, t["bias2"])
         assert_close(out1[n:n + 1], ref, f"pool-reduce full n={n}")
+
+
+def test_cout16_misaligned_input(ig3):
+    # x one float past a 16-byte boundary: the tensor-core path still runs (the kernel
+    # that copies 16-byte channel rows needs an aligned x, the other one does not).
+    wl = si.conv3d_workload("t", 1, 8, 5, 10, 64, 16, seed=93, epilogue="tanh_mish")
+    t = wl.generate_all()
+    ref = oracle.conv3d_tanh_mish(t["x"], t["w"], t["b"])
+    xs = torch.zeros(t["x"].size + 1, device="cuda")
+    xs[1:] = to_dev(t["x"]).reshape(-1)
+    x = xs[1:].view(t["x"].shape)
+    assert x.data_ptr() % 16 != 0
+    out = ig3.conv3d_fused(x, to_dev(t["w"]), to_dev(t["b"]), epilogue="tanh_mish", path="tc")
+    assert ig3.ig3_last_device_status() == 0
+    assert_close(out.cpu().numpy(), ref, "misaligned x, Cout 16, tc")
 
 
 # ---------------------------------------------------------------- edges of the boundary

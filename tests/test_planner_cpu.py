@@ -3,6 +3,8 @@
 tests/planner_check.cu includes the conv3d planner (csrc/conv3d_tc.cu) and, for every
 work unit of every CTA, recomputes the indices the kernel uses (TMEM columns, slots, B
 blocks, A rows, shared-memory offsets, input copies) against the plan's buffers;
+tests/tc16_plan_check.cu does the same for the 16-output-channel kernel with A in tensor
+memory (slot ring and its wrapped runs, A stages, B blocks, raw input copies, partials);
 tests/dwsep_plan_check.cu does the same for the depthwise-separable planner (strips,
 shared-memory layout, TMEM ranges, tensor-map box and strides, row-copy coordinates).
 They need nvcc (host compilation only) but no GPU.
@@ -18,7 +20,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 
 
-@pytest.mark.parametrize("checker", ["planner_check.cu", "dwsep_plan_check.cu"])
+@pytest.mark.parametrize("checker", ["planner_check.cu", "tc16_plan_check.cu", "dwsep_plan_check.cu"])
 def test_planner_index_bounds(checker):
     nvcc = shutil.which("nvcc") or ("/usr/local/cuda/bin/nvcc" if os.path.exists("/usr/local/cuda/bin/nvcc") else None)
     if nvcc is None:
