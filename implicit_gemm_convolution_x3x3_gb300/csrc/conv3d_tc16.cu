@@ -71,7 +71,7 @@ constexpr int kEpiWarp0 = 8, kEpiWarps = 8, kEpiThreads = 32 * kEpiWarps;
 constexpr int kCout = 16;
 constexpr int kSlotCols = 3 * kCout;           // [kw=0 | kw=1 | kw=2] x 16
 constexpr int kKStepCols = 3 * 16;             // three kh tiles of [hi 8 | lo 8]
-constexpr int kAStages = 2;
+constexpr int kMaxAStages = 4;
 constexpr int kTmemCols = 512;
 constexpr int kMaxXStages = 6;
 constexpr int kBRows = 18 * kCout;             // [hi: kd 2,1,0 x kw 0,1,2 | lo: the same] x 16
@@ -93,6 +93,7 @@ struct Params {
   int units;
   int NPOS;     // positions per raw channel row: 128 + 2W
   int XS;       // raw stages
+  int AST;      // A stages in tensor memory
   float inv_div;
   uint32_t blob_bytes;
   uint32_t x_stage_bytes;  // [8 * KSS channels][PP planes][NPOS positions] floats
@@ -145,24 +146,34 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __all_sync(0xffffffffu, ok) != 0;
 }
 
+// mbarrier.try_wait with a suspend-time hint: the thread sleeps until the phase
+// completes or about `hint_ns` pass, so a waiting warp takes no issue slots.
+__device__ __forceinline__ bool try_wait_suspend(uint32_t bar_addr, uint32_t parity, uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar_addr), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+
 // A bounded wait for the roles off the tensor core's critical path (loader,
-// producers, epilogue): between polls the thread sleeps briefly, leaving issue
-// slots to the MMA-issuing thread, whose bookkeeping between two chunks is not
+// producers, epilogue): the thread is suspended in the barrier until the phase
+// completes (re-checking the abort flag and the time limit every ~20 us), leaving
+// issue slots to the MMA-issuing thread, whose bookkeeping between two chunks is not
 // hidden by the short MMA queue.  Same contract as mbar_wait_bounded.
 __device__ __noinline__ bool wait_relaxed(uint64_t* bar, uint32_t parity, const WaitCtl& ctl, volatile int* abort) {
   const uint32_t a = smem_addr(bar);
   if (test_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
-    __nanosleep(32);
-    if (test_wait(a, parity)) return true;
-    if ((i & 15u) == 0u) {
-      if (*abort) return false;
-      if (globaltimer_ns() - t0 > ctl.limit_ns) {
-        *abort = 1;
-        atomicOr(ctl.status, kDevStatusTimeout);
-        return false;
-      }
+  for (;;) {
+    if (try_wait_suspend(a, parity, 20000u)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > ctl.limit_ns) {
+      *abort = 1;
+      atomicOr(ctl.status, kDevStatusTimeout);
+      return false;
     }
   }
 }
@@ -171,6 +182,40 @@ __device__ __forceinline__ bool warp_wait_relaxed(uint64_t* bar, uint32_t parity
                                                   volatile int* abort) {
   const bool ok = wait_relaxed(bar, parity, ctl, abort);
   return __all_sync(0xffffffffu, ok) != 0;
+}
+
+// Tests of PP + 1 barrier phases in one asm block, so that their shared-memory
+// latencies overlap: r[i] = phase par[i] of bar[i] completed (i < PP), r[PP] = phase
+// last_par of last_bar completed.
+template <int PP>
+__device__ __forceinline__ void test_wait_n(const uint32_t (&bar)[PP], const uint32_t (&par)[PP], uint32_t last_bar,
+                                            uint32_t last_par, bool (&r)[PP + 1]) {
+  uint32_t d0, d1 = 1, d2;
+  if constexpr (PP == 1) {
+    asm volatile(
+        "{\n\t.reg .pred p0, p2;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p0, [%2], %3;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p2, [%4], %5;\n\t"
+        "selp.u32 %0, 1, 0, p0;\n\tselp.u32 %1, 1, 0, p2;\n\t}"
+        : "=r"(d0), "=r"(d2)
+        : "r"(bar[0]), "r"(par[0]), "r"(last_bar), "r"(last_par)
+        : "memory");
+    r[0] = d0 != 0;
+    r[1] = d2 != 0;
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p0, p1, p2;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p0, [%3], %4;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p1, [%5], %6;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p2, [%7], %8;\n\t"
+        "selp.u32 %0, 1, 0, p0;\n\tselp.u32 %1, 1, 0, p1;\n\tselp.u32 %2, 1, 0, p2;\n\t}"
+        : "=r"(d0), "=r"(d1), "=r"(d2)
+        : "r"(bar[0]), "r"(par[0]), "r"(bar[PP - 1]), "r"(par[PP - 1]), "r"(last_bar), "r"(last_par)
+        : "memory");
+    r[0] = d0 != 0;
+    r[PP - 1] = d1 != 0;
+    r[PP] = d2 != 0;
+  }
 }
 
 // The issuing thread's wait, inline (a call in the issue loop slows every
@@ -366,9 +411,9 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc16_kernel(const Params p
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
   uint64_t* w_full = bars;
   uint64_t* mma_done = bars + 1;
-  uint64_t* a_full = bars + 2;                 // [kAStages]
-  uint64_t* a_empty = a_full + kAStages;       // [kAStages]
-  uint64_t* x_full = a_empty + kAStages;       // [XS]
+  uint64_t* a_full = bars + 2;                 // [AST]
+  uint64_t* a_empty = a_full + p.AST;          // [AST]
+  uint64_t* x_full = a_empty + p.AST;          // [XS]
   uint64_t* x_empty = x_full + p.XS;           // [XS]
   uint64_t* acc_full = x_empty + p.XS;         // [NSLOT]
   uint64_t* acc_empty = acc_full + p.NSLOT;    // [NSLOT]
@@ -383,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc16_kernel(const Params p
     s_abort = 0;
     mbar_init(w_full, 1);
     mbar_init(mma_done, 1);
-    for (int i = 0; i < kAStages; ++i) {
+    for (int i = 0; i < p.AST; ++i) {
       mbar_init(&a_full[i], kProdWarps);
       mbar_init(&a_empty[i], 1);
     }
@@ -510,13 +555,25 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc16_kernel(const Params p
         // Look ahead while those MMAs execute.
         const bool have_n = next_chunk<PP, KSS>(p, it, nxt, tmem_base, b_desc0, idesc0, idesc_slot);
         Ring ra_n = ra;
-        ra_n.next(kAStages);
+        ra_n.next((uint32_t)p.AST);
+        // The next chunk's barriers, tested in one go (the tests' latencies overlap):
+        // the slots its planes open (an unused test reads a completed phase of the
+        // A barrier instead) and its A stage.
         bool rdy[PP + 1];
+        {
+          const uint32_t a_bar = smem_addr(&a_full[ra_n.idx]);
+          uint32_t bar[PP], par[PP];
 #pragma unroll
-        for (int pi = 0; pi < PP; ++pi)
-          rdy[pi] = !have_n || !nxt.opens[pi] ||
-                    test_wait(smem_addr(&acc_empty[nxt.open_slot[pi]]), ((empty_par >> nxt.open_slot[pi]) & 1u) ^ 1u);
-        rdy[PP] = !have_n || test_wait(smem_addr(&a_full[ra_n.idx]), ra_n.phase);
+          for (int pi = 0; pi < PP; ++pi) {
+            const bool t = have_n && nxt.opens[pi];
+            bar[pi] = t ? smem_addr(&acc_empty[nxt.open_slot[pi]]) : a_bar;
+            par[pi] = t ? (((empty_par >> nxt.open_slot[pi]) & 1u) ^ 1u) : (ra_n.phase ^ 1u);
+          }
+          test_wait_n<PP>(bar, par, a_bar, ra_n.phase, rdy);
+#pragma unroll
+          for (int pi = 0; pi < PP; ++pi) rdy[pi] = rdy[pi] || !(have_n && nxt.opens[pi]);
+          rdy[PP] = rdy[PP] || !have_n;
+        }
         // Orders the next chunk's MMAs after the syncs just observed (the fence costs
         // the issuing thread a few hundred cycles: taken here, the queue covers it).
         tc_fence_after();
@@ -598,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc16_kernel(const Params p
             mbar_arrive(&a_full[ra.idx]);
           }
           rx.next((uint32_t)p.XS);
-          ra.next(kAStages);
+          ra.next((uint32_t)p.AST);
         }
       }
     }
@@ -814,8 +871,11 @@ struct Plan {
 
 size_t blob_bytes_for(int KS) { return (size_t)3 * KS * kBBlockBytes; }
 
-// Chunk shapes the kernel is instantiated for: (K-steps, input planes) per A stage.
-constexpr int kShapes[][2] = {{2, 1}, {1, 2}, {1, 1}};
+// Chunk shapes the kernel is instantiated for: (K-steps, input planes) per A stage,
+// and the number of A stages.  18 MMAs per chunk measured best: one plane of one
+// K-step with three A stages ran pool-reduce at the same speed and the 16-channel
+// sweep 17% slower than two K-steps of one plane with two stages.
+constexpr int kShapes[][3] = {{2, 1, 2}, {1, 2, 2}, {1, 1, 2}};
 
 // Cycles of one work unit of `planes` output planes: per input plane and K-step,
 // nine MMAs (three kh x three split products) of N = 48 * nkd, about
@@ -859,20 +919,20 @@ Plan make_plan_uncached(int N, int Cin, int D, int H, int W, int Cout, int epi, 
   const int step = (epi == IG3_EPI_POOL_REDUCE) ? 2 : 1;
   double best = 1e300;
   for (const auto& shape : kShapes) {
-    const int kss = shape[0], pp = shape[1];
+    const int kss = shape[0], pp = shape[1], ast = shape[2];
     if (kss == 2 && ks0 == 1) continue;
     const int KS = (ks0 + kss - 1) / kss * kss;
     const int nchunks = KS / kss;
     const uint32_t blob = (uint32_t)blob_bytes_for(KS);
     const uint32_t x_stage = (uint32_t)(pp * 8 * kss) * npos * 4u;
-    const int a_cols = kAStages * pp * kss * kKStepCols;
+    const int a_cols = ast * pp * kss * kKStepCols;
     const int nslot = (kTmemCols - a_cols) / kSlotCols;
     // A chunk's windows span pp + 2 slots; at least one more lets the MMAs run ahead.
     if (nslot < pp + 3) continue;
     const uint32_t off_x = (blob + 1023u) / 1024u * 1024u;
     // static shared memory (~11.3 KB), alignment and barriers
     const long long avail =
-        (long long)kSmemLimit - off_x - 12 * 1024 - (2 + 2 * kAStages + 2 * kMaxXStages + 2 * nslot) * 8;
+        (long long)kSmemLimit - off_x - 12 * 1024 - (2 + 2 * ast + 2 * kMaxXStages + 2 * nslot) * 8;
     const int xs = (int)std::min<long long>(kMaxXStages, avail / (long long)x_stage);
     if (xs < 2) continue;
     for (int P = OD - (OD % step); P >= step; P -= step) {
@@ -916,7 +976,8 @@ Plan make_plan_uncached(int N, int Cin, int D, int H, int W, int Cout, int epi, 
         p.a_col0 = (uint32_t)(nslot * kSlotCols);
         pl.kss = kss;
         pl.pp = pp;
-        pl.smem = std::max<size_t>(p.off_bar + (size_t)(2 + 2 * kAStages + 2 * xs + 2 * nslot) * 8, kMinSmem);
+        p.AST = ast;
+        pl.smem = std::max<size_t>(p.off_bar + (size_t)(2 + 2 * ast + 2 * xs + 2 * nslot) * 8, kMinSmem);
         pl.ok = true;
       }
     }

@@ -23,6 +23,8 @@ void check(int N, int Cin, int D, int H, int W, int epi, int sms, bool verbose) 
   const Params& p = pl.prm;
   const int KSS = pl.kss, PP = pl.pp;
   if (verbose)
+    printf("AST=%d ", p.AST);
+  if (verbose)
     printf("N%d Cin%d D%d H%d W%d epi%d: KSS=%d PP=%d KS=%d nch=%d NSLOT=%d G=%d S=%d P=%d units=%d NPOS=%d XS=%d smem=%zu\n",
            N, Cin, D, H, W, epi, KSS, PP, p.KS, p.nchunks, p.NSLOT, p.G, p.S, p.P, p.units, p.NPOS, p.XS, pl.smem);
   CHECK((KSS == 1 && PP == 2) || (KSS == 2 && PP == 1) || (KSS == 1 && PP == 1), "chunk shape");
@@ -32,14 +34,15 @@ void check(int N, int Cin, int D, int H, int W, int epi, int sms, bool verbose) 
   CHECK(p.KS % KSS == 0 && p.nchunks * KSS == p.KS, "chunks");
   CHECK(8 * p.KS >= Cin && 8 * (p.KS - KSS) < Cin, "K-steps cover Cin without an empty chunk");
   CHECK(p.a_col0 == (uint32_t)(p.NSLOT * kSlotCols), "a_col0");
-  CHECK(p.a_col0 + (uint32_t)(kAStages * PP * KSS * kKStepCols) <= (uint32_t)kTmemCols, "tmem cols");
+  CHECK(p.AST >= 2 && p.AST <= kMaxAStages, "A stages");
+  CHECK(p.a_col0 + (uint32_t)(p.AST * PP * KSS * kKStepCols) <= (uint32_t)kTmemCols, "tmem cols");
   CHECK(p.NSLOT >= PP + 3 && p.NSLOT <= 32, "nslot %d", p.NSLOT);
   CHECK(p.blob_bytes == blob_bytes_for(p.KS), "blob bytes");
   CHECK(p.off_x % 1024 == 0 && p.off_x >= p.blob_bytes, "x ring start");
   CHECK(p.x_stage_bytes == (uint32_t)(PP * 8 * KSS) * p.NPOS * 4 && p.x_stage_bytes % 16 == 0, "x stage");
   CHECK(p.off_bar == p.off_x + (uint32_t)p.XS * p.x_stage_bytes && p.off_bar % 8 == 0, "bars");
   CHECK(p.XS >= 2 && p.XS <= kMaxXStages, "xs");
-  CHECK(p.off_bar + (size_t)(2 + 2 * kAStages + 2 * p.XS + 2 * p.NSLOT) * 8 <= pl.smem, "bars beyond smem");
+  CHECK(p.off_bar + (size_t)(2 + 2 * p.AST + 2 * p.XS + 2 * p.NSLOT) * 8 <= pl.smem, "bars beyond smem");
   CHECK(pl.smem + 12288 <= (size_t)kSmemLimit, "dynamic + static shared memory %zu", pl.smem);
   CHECK(p.NPOS == 128 + 2 * W && (p.NPOS * 4) % 16 == 0, "npos");
   CHECK(p.G * 128 >= p.OH * W && (p.G - 1) * 128 < p.OH * W, "tiles cover");
@@ -78,7 +81,7 @@ void check(int N, int Cin, int D, int H, int W, int epi, int sms, bool verbose) 
         CHECK(p.NPOS <= 256 && PP <= 256 && 8 * KSS <= 256, "box dims");
         CHECK((long long)p.x_stage_bytes < (1 << 20), "tx count");
         for (int pi = 0; pi < npl; ++pi)
-          CHECK(p.a_col0 + (uint32_t)(kAStages - 1) * PP * KSS * kKStepCols + (uint32_t)((pi * KSS + KSS) * kKStepCols) <=
+          CHECK(p.a_col0 + (uint32_t)(p.AST - 1) * PP * KSS * kKStepCols + (uint32_t)((pi * KSS + KSS) * kKStepCols) <=
                     (uint32_t)kTmemCols, "A cols");
         // producer reads: rows (c * PP + pi) of NPOS, positions m + kh*W < 128 + 2W
         CHECK((8 * KSS - 1) * PP + (PP - 1) < 8 * KSS * PP && 127 + 2 * W < p.NPOS, "producer reads");
