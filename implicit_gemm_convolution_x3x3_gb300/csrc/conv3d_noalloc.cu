@@ -14,7 +14,9 @@
 // not pass the array's name to a kernel (in host code it names a host-side stand-in,
 // not device memory), so the first call on each device looks up the array's device
 // address with cudaGetSymbolAddress while that device is current, and later calls
-// reuse it.
+// reuse it.  The address belongs to the context it was looked up in: when the
+// current context is another one (after a cudaDeviceReset, say), the next call
+// looks it up again.
 #include <mutex>
 
 #include "ig3_internal.h"
@@ -25,6 +27,7 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[IG3_NOALLOC_SCR
 
 constexpr int kMaxDevices = 64;
 void* g_scratch_addr[kMaxDevices];
+void* g_scratch_ctx[kMaxDevices];  // the context each address was looked up in
 std::mutex g_scratch_mu;
 
 // Device address of g_noalloc_scratch on the current device (looked up once per
@@ -41,15 +44,18 @@ void* scratch_on_current_device() {
     return nullptr;
   }
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  void* ctx = ig3::current_context();
+  if (g_scratch_addr[dev] == nullptr || ctx == nullptr || ctx != g_scratch_ctx[dev]) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess || p == nullptr) {
+      g_scratch_addr[dev] = nullptr;
       ig3::cuda_status(e != cudaSuccess ? e : cudaErrorInvalidSymbol,
                        "conv3d_fused_noalloc: cudaGetSymbolAddress of the static scratch");
       return nullptr;
     }
     g_scratch_addr[dev] = p;
+    g_scratch_ctx[dev] = ig3::current_context();  // now initialised by the lookup
   }
   return g_scratch_addr[dev];
 }

@@ -27,6 +27,7 @@ std::atomic<unsigned long long> g_launches{0};
 
 struct DeviceInfo {
   bool ready = false;
+  void* ctx = nullptr;  // the context the address below belongs to
   unsigned int* status = nullptr;
   int sms = 0;
 };
@@ -34,19 +35,23 @@ constexpr int kMaxDevices = 64;
 DeviceInfo g_devices[kMaxDevices];
 std::mutex g_devices_mu;
 
-// Set-up of the current device, once: the status word's device address and the SM count.
+// Set-up of the current device: the status word's device address and the SM count,
+// looked up once per context (a cudaDeviceReset makes a new context, in which the
+// module's variables may sit at other addresses).
 DeviceInfo* current_device() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> lock(g_devices_mu);
   DeviceInfo& d = g_devices[dev];
-  if (!d.ready) {
+  void* ctx = current_context();
+  if (!d.ready || ctx == nullptr || ctx != d.ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_ig3_device_status) != cudaSuccess) return nullptr;
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return nullptr;
     d.status = static_cast<unsigned int*>(p);
     d.sms = sms;
+    d.ctx = current_context();  // now initialised by the lookup
     d.ready = true;
   }
   return &d;
@@ -159,6 +164,22 @@ WaitCtl wait_ctl() {
   c.limit_ns = ns ? ns : kDefaultWaitNs;
   DeviceInfo* d = current_device();
   c.status = d ? d->status : nullptr;
+  return c;
+}
+
+void* current_context() {
+  using Fn = CUresult (*)(CUcontext*);
+  static std::once_flag once;
+  static Fn fn = nullptr;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<Fn>(ptr);
+  });
+  CUcontext c = nullptr;
+  if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
   return c;
 }
 

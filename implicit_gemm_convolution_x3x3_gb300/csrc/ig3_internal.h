@@ -55,6 +55,10 @@ int count_launch(int status);
 WaitCtl wait_ctl();
 // Number of SMs of the current device (cached).
 int num_sms();
+// The calling thread's current CUDA context (through the driver entry point), or
+// nullptr if none is current yet.  Device addresses of the library's __device__
+// variables are valid within one context.
+void* current_context();
 // The driver's tensor-map encoder, looked up once through the runtime (no link-time
 // dependency on the driver library); nullptr if unavailable.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();

@@ -172,7 +172,9 @@ int conv3d_fused_ex(const float* x, int N, int Cin, int D, int H, int W, int pad
  *     rejected with IG3_ERR_WORKSPACE before anything is launched.
  *   - The first call on each device looks up the buffer's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is valid in the context it was
+ *     looked up in: after a cudaDeviceReset (a new context) the next call looks it
+ *     up again, so make that call before any capture too.
  *   - Every call on a device shares the one buffer, and it keeps the last call's
  *     contents.  No part of it needs to start at zero (each call rewrites all it
  *     reads), but calls whose work overlaps on the GPU (different streams, or

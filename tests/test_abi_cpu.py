@@ -52,6 +52,22 @@ def test_python_binding_lists_every_symbol():
     assert sorted(m.EXPORTED_SYMBOLS) == declared_functions()
 
 
+def test_noalloc_scratch_size_matches_header():
+    # The binding's NOALLOC_SCRATCH_BYTES is what the tests size their shapes by: it
+    # must be the header's IG3_NOALLOC_SCRATCH_BYTES, the size of the library's buffer.
+    import sys
+    sys.path.insert(0, ROOT)
+    pytest.importorskip("torch")
+    _build_if_needed()
+    import implicit_gemm_convolution_x3x3_gb300 as m
+    text = open(HEADER).read()
+    mt = re.search(r"#define\s+IG3_NOALLOC_SCRATCH_BYTES\s+\(([^)]*)\)", text)
+    assert mt, "IG3_NOALLOC_SCRATCH_BYTES not found in ig3.h"
+    expr = mt.group(1).replace("u", "")
+    assert re.fullmatch(r"[0-9*+ ]+", expr), expr
+    assert eval(expr) == m.NOALLOC_SCRATCH_BYTES
+
+
 def _c(lib):
     f = lib.conv3d_fused
     f.restype = ctypes.c_int

@@ -192,9 +192,26 @@ def test_pool_reduce_full_size_sampled_and_deterministic(ig3):
     assert ig3.ig3_last_device_status() == 0
     assert out1.shape == (128,)
     assert np.array_equal(out1, out2), "pool-reduce is not deterministic"
-    for n in (0, 1, 64, 127):
-        ref = oracle.conv3d_pool_reduce(t["x"][n:n + 1], t["w"], t["b"], 2.0, 2, t["bias2"])
-        assert_close(out1[n:n + 1], ref, f"pool-reduce full n={n}")
+    # Every one of the 128 outputs against the oracle (47.6 GFLOP of float64 work).
+    ref = oracle.conv3d_pool_reduce(t["x"], t["w"], t["b"], 2.0, 2, t["bias2"])
+    assert_close(out1, ref, "pool-reduce full size, all outputs")
+
+
+def test_headline_full_size_every_element(ig3):
+    # The conv3d + tanh(mish) workload in the benchmark's launch configuration,
+    # compared with the oracle on every one of its 118,087,680 outputs (one batch
+    # item of the oracle at a time).
+    wl = si.conv3d_tanh_mish()
+    t = wl.generate_all()
+    x = to_dev(t["x"]); w = to_dev(t["w"]); b = to_dev(t["b"])
+    out = ig3.conv3d_fused(x, w, b, epilogue="tanh_mish")
+    assert ig3.ig3_last_device_status() == 0
+    got = out.cpu().numpy()
+    del x, w, b, out
+    torch.cuda.empty_cache()
+    for n in range(got.shape[0]):
+        ref = oracle.conv3d_tanh_mish(t["x"][n:n + 1], t["w"], t["b"])
+        assert_close(got[n:n + 1], ref, f"conv3d + tanh(mish) full size, batch item {n}")
 
 
 def test_cout16_misaligned_input(ig3):
