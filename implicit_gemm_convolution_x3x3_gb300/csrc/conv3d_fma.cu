@@ -10,6 +10,9 @@
 // 4cg..4cg+3 -> 64 accumulators.  A warp is one channel group, so its weight reads
 // are shared-memory broadcasts; its input reads are float4 rows (conflict free).
 // Input channels are staged 4 at a time: a (2+2) x (8+2) x (32+2) halo per channel.
+// With zero padding P (the padding discussion of the same page: input coordinate
+// od + kd - P, zero outside x, output D + 2P - 2) the staging reads the halo at the
+// shifted coordinates and writes zeros outside x; nothing else changes.
 //
 // The 2x2x2 output block of a thread is exactly one pooling window per column pair,
 // so the pool-reduce epilogue ("Kimi-K2.6__l2_p8": /2, MaxPool3d(2), global mean,
@@ -27,12 +30,13 @@ constexpr int kInW = kTW + 2, kInWPad = 36, kInH = kTH + 2, kInD = kTD + 2;
 template <int EPI>
 __global__ void __launch_bounds__(kThreads) conv3d_fma_kernel(
     const float* __restrict__ x, const float* __restrict__ w, const float* __restrict__ bias,
-    float* __restrict__ y, float* __restrict__ partial, int N, int Cin, int D, int H, int W, int Cout,
+    float* __restrict__ y, float* __restrict__ partial, int N, int Cin, int D, int H, int W, int P, int Cout,
     float inv_div) {
   __shared__ __align__(16) float s_in[kCC][kInD][kInH][kInWPad];
   __shared__ __align__(16) float s_w[kCC][27][kTCO];
 
-  const int OD = D - 2, OH = H - 2, OW = W - 2;
+  // Zero padding P: output od reads input planes od + kd - P (zero outside x).
+  const int OD = D + 2 * P - 2, OH = H + 2 * P - 2, OW = W + 2 * P - 2;
   const int tiles_w = (OW + kTW - 1) / kTW;
   const int ow0 = (blockIdx.x % tiles_w) * kTW;
   const int oh0 = (blockIdx.x / tiles_w) * kTH;
@@ -63,9 +67,9 @@ __global__ void __launch_bounds__(kThreads) conv3d_fma_kernel(
       r /= kInH;
       const int xd = r % kInD;
       const int c = r / kInD;
-      const int gc = c0 + c, gd = od0 + xd, gh = oh0 + xh, gw = ow0 + xw;
+      const int gc = c0 + c, gd = od0 + xd - P, gh = oh0 + xh - P, gw = ow0 + xw - P;
       float v = 0.0f;
-      if (gc < Cin && gd < D && gh < H && gw < W)
+      if (gc < Cin && (unsigned)gd < (unsigned)D && (unsigned)gh < (unsigned)H && (unsigned)gw < (unsigned)W)
         v = __ldg(&x[((size_t)n * Cin + gc) * D * plane + (size_t)gd * plane + (size_t)gh * W + gw]);
       s_in[c][xd][xh][xw] = v;
     }
@@ -224,15 +228,15 @@ int conv3d_fma_launch(const Conv3dArgs& a) {
   switch (a.epi) {
     case IG3_EPI_NONE:
       conv3d_fma_kernel<IG3_EPI_NONE><<<g, kThreads, 0, a.stream>>>(a.x, a.w, a.b, a.y, nullptr, a.N, a.Cin, a.D,
-                                                                    a.H, a.W, a.Cout, inv_div);
+                                                                    a.H, a.W, a.pad, a.Cout, inv_div);
       break;
     case IG3_EPI_TANH_MISH:
       conv3d_fma_kernel<IG3_EPI_TANH_MISH><<<g, kThreads, 0, a.stream>>>(a.x, a.w, a.b, a.y, nullptr, a.N, a.Cin,
-                                                                         a.D, a.H, a.W, a.Cout, inv_div);
+                                                                         a.D, a.H, a.W, a.pad, a.Cout, inv_div);
       break;
     default:
       conv3d_fma_kernel<IG3_EPI_POOL_REDUCE><<<g, kThreads, 0, a.stream>>>(a.x, a.w, a.b, nullptr, partial, a.N,
-                                                                           a.Cin, a.D, a.H, a.W, a.Cout, inv_div);
+                                                                           a.Cin, a.D, a.H, a.W, a.pad, a.Cout, inv_div);
       break;
   }
   int st = count_launch(cuda_status(cudaGetLastError(), "conv3d FMA kernel launch"));

@@ -201,7 +201,14 @@ double unit_cycles(int kdm, int hl, int planes, int Cout, int KS, int nchunks, i
   return c;
 }
 
-Plan make_plan_uncached(int N, int Cin, int D, int H, int W, int Cout, int epi, int sms) {
+// flags: kNoKwWindow keeps the kd x kw window (KDM 9) out of the plan.  Its epilogue
+// takes the kw = 1, 2 blocks of a row's last two positions from outside the tile, so
+// it relies on those two columns being the discarded wrap-around columns of a valid
+// convolution; with zero padding on chip the stored columns are shifted and can
+// include them.
+enum : int { kNoKwWindow = 1 };
+
+Plan make_plan_uncached(int N, int Cin, int D, int H, int W, int Cout, int epi, int sms, int flags) {
   Plan pl;
   if (Cout % 16 != 0 || Cout > 128) {
     pl.why = "Cout must be a multiple of 16 and at most 128";
@@ -219,7 +226,7 @@ Plan make_plan_uncached(int N, int Cin, int D, int H, int W, int Cout, int epi, 
   // Cout 16 with tiles of whole input rows (W divides 128): kw joins kd inside the
   // MMA's N (the epilogue's shifted sum never crosses a tile).  Not for pool-reduce:
   // its epilogue, not the MMAs, bounds it, and the shift exchange adds to it.
-  const int kdm = (epi != IG3_EPI_POOL_REDUCE && Cout == 16 && W <= 128 && 128 % W == 0) ? 9
+  const int kdm = (epi != IG3_EPI_POOL_REDUCE && Cout == 16 && W <= 128 && 128 % W == 0 && !(flags & kNoKwWindow)) ? 9
                   : (3 * Cout <= 256)                                                      ? 3
                                                                                            : 1;
   const int hl = (kdm == 3 && 6 * Cout <= 256) ? 1 : 0;
@@ -332,17 +339,17 @@ Plan make_plan_uncached(int N, int Cin, int D, int H, int W, int Cout, int epi, 
 
 // Plans are cached per (shape, epilogue, SM count): the search above simulates the
 // persistent schedule and is not free.
-Plan make_plan(int N, int Cin, int D, int H, int W, int Cout, int epi, int sms) {
-  using Key = std::array<int, 8>;
+Plan make_plan(int N, int Cin, int D, int H, int W, int Cout, int epi, int sms, int flags = 0) {
+  using Key = std::array<int, 9>;
   static std::mutex mu;
   static std::map<Key, Plan> cache;
-  const Key key{N, Cin, D, H, W, Cout, epi, sms};
+  const Key key{N, Cin, D, H, W, Cout, epi, sms, flags};
   {
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
   }
-  Plan pl = make_plan_uncached(N, Cin, D, H, W, Cout, epi, sms);
+  Plan pl = make_plan_uncached(N, Cin, D, H, W, Cout, epi, sms, flags);
   std::lock_guard<std::mutex> lock(mu);
   if (cache.size() > 256) cache.clear();
   cache.emplace(key, pl);
@@ -359,7 +366,40 @@ const char* conv3d_tc_unsupported_reason(int N, int Cin, int D, int H, int W, in
   return buf;
 }
 
+// Zero padding on chip: the kernel runs the valid convolution over a virtual padded
+// volume.  When the convert can load aligned quads (W % 4 == 0, x 16-byte aligned,
+// pad <= 4, and not pool-reduce, whose 2x2 pairs need stored and virtual columns of
+// the same parity) virtual column 0 is real column -4 and the row pitch W plus
+// pad + 2 rounded up to 4 (so that the last stored output, at virtual column
+// W + pad + 1, lies inside the row); else column 0 is real column -pad and the pitch
+// W + 2*pad.  Either way every position a stored output reads beyond the real row
+// (the right border) is inside the row or the next virtual row's left border, which
+// is zero.
+struct VirtualDims {
+  int D, H, W, col0;
+  bool vec;
+};
+VirtualDims virtual_dims(const Conv3dArgs& a, bool x_aligned) {
+  VirtualDims v{a.D + 2 * a.pad, a.H + 2 * a.pad, a.W + 2 * a.pad, a.pad, false};
+  if (a.pad > 0 && x_aligned && a.W % 4 == 0 && a.pad <= 4 && a.epi != IG3_EPI_POOL_REDUCE) {
+    v.W = a.W + (a.pad + 2 + 3) / 4 * 4;
+    v.col0 = 4;
+    v.vec = true;
+  }
+  return v;
+}
+
 size_t conv3d_tc_workspace(const Conv3dArgs& a) {
+  if (a.pad > 0) {
+    // Sized for either virtual pitch (the choice depends on x's alignment at the call).
+    size_t ws = 0;
+    for (bool aligned : {false, true}) {
+      const VirtualDims v = virtual_dims(a, aligned);
+      Plan pl = make_plan(a.N, a.Cin, v.D, v.H, v.W, a.Cout, a.epi, 148, kNoKwWindow);
+      if (pl.ok) ws = std::max(ws, pl.blob_bytes + pl.partial_bytes);
+    }
+    return ws;
+  }
   Plan pl = make_plan(a.N, a.Cin, a.D, a.H, a.W, a.Cout, a.epi, 148);
   const size_t own = pl.ok ? pl.blob_bytes + pl.partial_bytes : 0;
   // Either kernel may run (the A-in-tensor-memory one needs x 16-byte aligned).
@@ -367,10 +407,12 @@ size_t conv3d_tc_workspace(const Conv3dArgs& a) {
 }
 
 int conv3d_tc_launch(const Conv3dArgs& a) {
-  if (reinterpret_cast<uintptr_t>(a.x) % 16 == 0 && conv3d_tc16_applies(a, nullptr)) return conv3d_tc16_launch(a);
+  const bool x_aligned = reinterpret_cast<uintptr_t>(a.x) % 16 == 0;
+  if (a.pad == 0 && x_aligned && conv3d_tc16_applies(a, nullptr)) return conv3d_tc16_launch(a);
   const int sms = num_sms();
   if (sms <= 0) return fail(IG3_ERR_CUDA, "conv3d TC path: cannot query the SM count");
-  Plan pl = make_plan(a.N, a.Cin, a.D, a.H, a.W, a.Cout, a.epi, sms);
+  const VirtualDims vd = virtual_dims(a, x_aligned);
+  Plan pl = make_plan(a.N, a.Cin, vd.D, vd.H, vd.W, a.Cout, a.epi, sms, a.pad > 0 ? kNoKwWindow : 0);
   if (!pl.ok) return fail(IG3_ERR_UNSUPPORTED, "conv3d TC path: %s", pl.why);
   TcParams p = pl.prm;
   uint8_t* ws = static_cast<uint8_t*>(a.ws);
@@ -380,8 +422,20 @@ int conv3d_tc_launch(const Conv3dArgs& a) {
   p.y = a.y;
   p.partial = reinterpret_cast<float*>(ws + pl.blob_bytes);
   p.inv_div = (a.epi == IG3_EPI_POOL_REDUCE) ? 1.0f / a.divisor : 1.0f;
-  p.vec = ((size_t)a.H * a.W % 4 == 0 && reinterpret_cast<uintptr_t>(a.x) % 16 == 0) ? 1 : 0;
-  if (!p.vec) p.XS = 0;  // bulk copies need 16-byte aligned rows
+  if (a.pad == 0) {
+    p.vec = ((size_t)a.H * a.W % 4 == 0 && x_aligned) ? 1 : 0;
+    if (!p.vec) p.XS = 0;  // bulk copies need 16-byte aligned rows
+  } else {
+    p.pad = a.pad;
+    p.Dr = a.D;
+    p.Hr = a.H;
+    p.Wr = a.W;
+    p.col0 = vd.col0;
+    p.ow_off = vd.col0 - a.pad;
+    p.OW = a.OW();
+    p.vec = vd.vec ? 1 : 0;
+    p.XS = 0;  // the convert warps load x themselves and fill the border
+  }
   p.ctl = wait_ctl();
   if (!p.ctl.status) return fail(IG3_ERR_CUDA, "conv3d TC path: device status word unavailable");
 

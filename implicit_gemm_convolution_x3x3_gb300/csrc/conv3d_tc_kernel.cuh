@@ -44,7 +44,13 @@ struct TcParams {
   int SB;        // weight ring stages (streaming)
   int XS;        // raw input stages of the bulk-copy loader (0: convert warps load x)
   int epi;
-  int vec;       // x planes 16-byte aligned with H*W % 4 == 0: convert with 16-byte loads
+  int vec;       // convert with 16-byte loads (aligned quads of positions)
+  // Zero padding on chip.  With pad > 0 the kernel runs the valid convolution over a
+  // virtual padded volume of D x H x W (W the virtual row pitch) whose position
+  // (plane d, row h, column v) holds x[d - pad][h - pad][v - col0] of the real
+  // Dr x Hr x Wr input, zero outside it; the convert warps fill the zeros.  Output
+  // column v of a virtual row is stored at column v - ow_off (OW stored columns).
+  int pad, Dr, Hr, Wr, col0, ow_off;
   float inv_div;
   uint32_t a_half_bytes;   // one of hi / lo in an A stage
   uint32_t a_stage_bytes;  // hi + lo
@@ -97,6 +103,21 @@ static __host__ __device__ __forceinline__ uint32_t slot_add(const TcParams& p, 
 static __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& ctl, volatile int* abort) {
   const bool ok = mbar_wait_bounded(bar, parity, ctl, abort);
   return __all_sync(0xffffffffu, ok) != 0;
+}
+
+// Address of virtual position pos (= h * W + v) of virtual input plane d, channel 0 of
+// batch item n, in the real input; nullptr where the position lies in the zero
+// border (or past the virtual plane).  The division by the pitch is exact for
+// pos < 2^24.
+static __device__ __forceinline__ const float* padded_src(const TcParams& p, int n, int d, int pos) {
+  int h = __float2int_rz(__fdividef((float)pos, (float)p.W));
+  int v = pos - h * p.W;
+  if (v < 0) { --h; v += p.W; }
+  else if (v >= p.W) { ++h; v -= p.W; }
+  const int dr = d - p.pad, hr = h - p.pad, wr = v - p.col0;
+  if ((unsigned)dr >= (unsigned)p.Dr || (unsigned)hr >= (unsigned)p.Hr || (unsigned)wr >= (unsigned)p.Wr)
+    return nullptr;
+  return p.x + (((size_t)n * p.Cin * p.Dr + dr) * p.Hr + hr) * (size_t)p.Wr + wr;
 }
 
 // Non-blocking test of a barrier phase.
@@ -585,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
             }
             mbar_arrive(&x_empty[rx.idx]);
             rx.next((uint32_t)p.XS);
-          } else if (p.vec) {
+          } else if (p.vec && p.pad == 0) {
             // Item = (channel group, 4 consecutive positions): four 16-byte loads (one
             // per channel, coalesced along positions), transposed in registers to four
             // [position][4 channels] entries.  H*W % 4 == 0, so a quad lies wholly inside
@@ -629,7 +650,52 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
                 }
               }
             }
-          } else
+          } else if (p.vec) {
+            // The same over the virtual padded volume: a quad of virtual positions is
+            // wholly inside x's row or wholly in the zero border (aligned quads).
+            const size_t cstride = (size_t)p.Dr * p.Hr * p.Wr;
+            const int quads = p.NPOS >> 2;
+            const int vitems = (CC / 4) * quads;
+            for (int i0 = ct; i0 < vitems; i0 += 2 * kConvThreads) {
+              float4 v[2][4];
+#pragma unroll
+              for (int k = 0; k < 2; ++k) {
+                const int i = i0 + k * kConvThreads;
+                const int grp = i / quads, qd = i - grp * quads;
+                const int pos = p0 + 4 * qd;
+                // The quad's source in the real input, or the zero border.
+                const float* src = padded_src(p, un.n, d, pos);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  const int c = c0 + grp * 4 + j;
+                  v[k][j] = (i < vitems && src != nullptr && c < p.Cin)
+                                ? __ldg(reinterpret_cast<const float4*>(src + (size_t)c * cstride))
+                                : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                }
+              }
+#pragma unroll
+              for (int k = 0; k < 2; ++k) {
+                const int i = i0 + k * kConvThreads;
+                if (i < vitems) {
+                  const int grp = i / quads, qd = i - grp * quads;
+                  const uint32_t off = (uint32_t)(grp * p.NPOS + 4 * qd) * 16u;
+                  float h[4][4], l[4][4];
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) {
+                    split_tf32(v[k][j].x, h[0][j], l[0][j]);
+                    split_tf32(v[k][j].y, h[1][j], l[1][j]);
+                    split_tf32(v[k][j].z, h[2][j], l[2][j]);
+                    split_tf32(v[k][j].w, h[3][j], l[3][j]);
+                  }
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    st_shared_v4(hi_base + off + 16u * e, h[e][0], h[e][1], h[e][2], h[e][3]);
+                    st_shared_v4(lo_base + off + 16u * e, l[e][0], l[e][1], l[e][2], l[e][3]);
+                  }
+                }
+              }
+            }
+          } else if (p.pad == 0) {
           for (int i0 = ct; i0 < items; i0 += 2 * kConvThreads) {
             float v[2][4];
 #pragma unroll
@@ -657,6 +723,37 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
                 st_shared_v4(lo_base + off, l[0], l[1], l[2], l[3]);
               }
             }
+          }
+          } else {
+          // Scalar loads over the virtual padded volume.
+          const size_t cstride = (size_t)p.Dr * p.Hr * p.Wr;
+          for (int i0 = ct; i0 < items; i0 += 2 * kConvThreads) {
+            float v[2][4];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const int i = i0 + k * kConvThreads;
+              const int grp = i / p.NPOS, pp = i - grp * p.NPOS;
+              const int pos = p0 + pp;
+              const float* src = padded_src(p, un.n, d, pos);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int c = c0 + grp * 4 + j;
+                v[k][j] = (i < items && src != nullptr && c < p.Cin) ? __ldg(src + (size_t)c * cstride) : 0.0f;
+              }
+            }
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const int i = i0 + k * kConvThreads;
+              if (i < items) {
+                const uint32_t off = (uint32_t)i * 16u;  // [group][position][4]
+                float h[4], l[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) split_tf32(v[k][j], h[j], l[j]);
+                st_shared_v4(hi_base + off, h[0], h[1], h[2], h[3]);
+                st_shared_v4(lo_base + off, l[0], l[1], l[2], l[3]);
+              }
+            }
+          }
           }
           fence_proxy_async_smem();
           mbar_arrive(&a_full[ra.idx]);
@@ -784,11 +881,11 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
             for (int j = 0; j < 8; ++j) v[t][j] += s1[t][j] + s2[t][j];
           // Tiles hold whole rows, so a lane has the same column in every tile.
           const int lq = q * 32 + lane;
-          const int ow = (p0 + lq) % p.W;
+          const int ow = (p0 + lq) % p.W - p.ow_off;
 #pragma unroll
           for (int t = 0; t < T; ++t) {
             const int oh = (p0 + t * 128 + lq) / p.W;
-            if (oh < p.OH && ow < p.OW) {
+            if (oh < p.OH && ow >= 0 && ow < p.OW) {
               float* yb = p.y + (((size_t)un.n * p.Cout + c0) * p.OD + od) * OHW + (size_t)oh * p.OW + ow;
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
@@ -805,8 +902,8 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
           const int c0 = (it - t * cchunks) * CW;
           const int lp = t * 128 + q * 32 + lane;  // position within the unit
           const int pos = p0 + lp;
-          const int oh = pos / p.W, ow = pos - oh * p.W;
-          const bool valid = (oh < p.OH) && (ow < p.OW);
+          const int oh = pos / p.W, ow = pos - oh * p.W - p.ow_off;
+          const bool valid = (oh < p.OH) && (ow >= 0) && (ow < p.OW);
           const uint32_t taddr = lane_base + (uint32_t)t * tile_cols + slot * slot_w + (uint32_t)c0;
           float v[CW];
           float bv[16];

@@ -220,6 +220,47 @@ int selftest_bounded_wait(unsigned long long timeout_ns, cudaStream_t stream) {
   return count_launch(cuda_status(cudaGetLastError(), "bounded-wait self-test launch"));
 }
 
+size_t conv3d_workspace(int N, int Cin, int D, int H, int W, int pad, int Cout, int epi, int path) {
+  const int p = conv3d_select_quiet(N, Cin, D + 2 * pad, H + 2 * pad, W + 2 * pad, Cout, epi, path);
+  if (p < 0) return 0;
+  Conv3dArgs a{};
+  a.N = N; a.Cin = Cin; a.D = D; a.H = H; a.W = W; a.pad = pad; a.Cout = Cout; a.epi = epi;
+  return p == IG3_PATH_TC ? conv3d_tc_workspace(a) : conv3d_fma_workspace(a);
+}
+
+int conv3d_run(const float* x, int N, int Cin, int D, int H, int W, int pad, const float* w, int Cout,
+               const float* b, int epilogue, const ig3_epi_params* params, float* y, void* workspace,
+               size_t workspace_bytes, int path, void* stream, const char* who) {
+  // Path choice and shape checks on the convolution's (padded) input volume.
+  const int p = conv3d_select(N, Cin, D + 2 * pad, H + 2 * pad, W + 2 * pad, Cout, epilogue, path);
+  if (p < 0) return p;
+  if (!x || !w || !y) return fail(IG3_ERR_INVALID_ARG, "%s: x, w and y must not be NULL", who);
+  Conv3dArgs a{};
+  a.x = x; a.N = N; a.Cin = Cin; a.D = D; a.H = H; a.W = W; a.pad = pad; a.w = w; a.Cout = Cout; a.b = b;
+  a.epi = epilogue; a.divisor = 1.0f; a.pool = 2; a.bias2 = nullptr; a.y = y;
+  a.ws = workspace; a.ws_bytes = workspace_bytes; a.stream = static_cast<cudaStream_t>(stream);
+  if (epilogue == IG3_EPI_POOL_REDUCE) {
+    if (!params || !params->bias2)
+      return fail(IG3_ERR_INVALID_ARG, "%s: POOL_REDUCE needs params with a bias2 pointer", who);
+    if (params->pool != 2) return fail(IG3_ERR_UNSUPPORTED, "%s: only pool = 2 is supported", who);
+    if (!std::isfinite(params->divisor) || params->divisor == 0.0f)
+      return fail(IG3_ERR_INVALID_ARG, "%s: divisor must be finite and nonzero", who);
+    a.divisor = params->divisor;
+    a.pool = params->pool;
+    a.bias2 = params->bias2;
+  }
+  const size_t need = (p == IG3_PATH_TC) ? conv3d_tc_workspace(a) : conv3d_fma_workspace(a);
+  if (need > 0) {
+    if (!workspace || workspace_bytes < need)
+      return fail(IG3_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", who, need,
+                  workspace ? workspace_bytes : (size_t)0);
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+      return fail(IG3_ERR_WORKSPACE, "%s: workspace must be 256-byte aligned", who);
+  }
+  if (!current_device()) return fail(IG3_ERR_CUDA, "%s: device set-up failed", who);
+  return p == IG3_PATH_TC ? conv3d_tc_launch(a) : conv3d_fma_launch(a);
+}
+
 }  // namespace ig3
 
 using namespace ig3;
@@ -227,11 +268,7 @@ using namespace ig3;
 extern "C" {
 
 size_t conv3d_fused_workspace_size(int N, int Cin, int D, int H, int W, int Cout, int epilogue, int path) {
-  const int p = ig3::conv3d_select_quiet(N, Cin, D, H, W, Cout, epilogue, path);
-  if (p < 0) return 0;
-  Conv3dArgs a{};
-  a.N = N; a.Cin = Cin; a.D = D; a.H = H; a.W = W; a.Cout = Cout; a.epi = epilogue;
-  return p == IG3_PATH_TC ? conv3d_tc_workspace(a) : conv3d_fma_workspace(a);
+  return conv3d_workspace(N, Cin, D, H, W, 0, Cout, epilogue, path);
 }
 
 int conv3d_fused_select_path(int N, int Cin, int D, int H, int W, int Cout, int epilogue, int path) {
@@ -245,33 +282,8 @@ int dwsep_conv2d_select_path(int N, int C, int H, int W, int Cout, int path) {
 int conv3d_fused(const float* x, int N, int Cin, int D, int H, int W, const float* w, int Cout, const float* b,
                  int epilogue, const ig3_epi_params* params, float* y, void* workspace, size_t workspace_bytes,
                  int path, void* stream) {
-  const int p = conv3d_select(N, Cin, D, H, W, Cout, epilogue, path);
-  if (p < 0) return p;
-  if (!x || !w || !y) return fail(IG3_ERR_INVALID_ARG, "conv3d_fused: x, w and y must not be NULL");
-  Conv3dArgs a{};
-  a.x = x; a.N = N; a.Cin = Cin; a.D = D; a.H = H; a.W = W; a.w = w; a.Cout = Cout; a.b = b;
-  a.epi = epilogue; a.divisor = 1.0f; a.pool = 2; a.bias2 = nullptr; a.y = y;
-  a.ws = workspace; a.ws_bytes = workspace_bytes; a.stream = static_cast<cudaStream_t>(stream);
-  if (epilogue == IG3_EPI_POOL_REDUCE) {
-    if (!params || !params->bias2)
-      return fail(IG3_ERR_INVALID_ARG, "conv3d_fused: POOL_REDUCE needs params with a bias2 pointer");
-    if (params->pool != 2) return fail(IG3_ERR_UNSUPPORTED, "conv3d_fused: only pool = 2 is supported");
-    if (!std::isfinite(params->divisor) || params->divisor == 0.0f)
-      return fail(IG3_ERR_INVALID_ARG, "conv3d_fused: divisor must be finite and nonzero");
-    a.divisor = params->divisor;
-    a.pool = params->pool;
-    a.bias2 = params->bias2;
-  }
-  const size_t need = (p == IG3_PATH_TC) ? conv3d_tc_workspace(a) : conv3d_fma_workspace(a);
-  if (need > 0) {
-    if (!workspace || workspace_bytes < need)
-      return fail(IG3_ERR_WORKSPACE, "conv3d_fused: workspace of %zu bytes needed, %zu given", need,
-                  workspace ? workspace_bytes : (size_t)0);
-    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
-      return fail(IG3_ERR_WORKSPACE, "conv3d_fused: workspace must be 256-byte aligned");
-  }
-  if (!current_device()) return fail(IG3_ERR_CUDA, "conv3d_fused: device set-up failed");
-  return p == IG3_PATH_TC ? conv3d_tc_launch(a) : conv3d_fma_launch(a);
+  return conv3d_run(x, N, Cin, D, H, W, 0, w, Cout, b, epilogue, params, y, workspace, workspace_bytes, path, stream,
+                    "conv3d_fused");
 }
 
 int dwsep_conv2d(const float* x, int N, int C, int H, int W, const float* w_dw, const float* w_pw, int Cout,

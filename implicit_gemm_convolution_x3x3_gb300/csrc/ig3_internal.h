@@ -15,7 +15,8 @@ namespace ig3 {
 
 struct Conv3dArgs {
   const float* x;
-  int N, Cin, D, H, W;
+  int N, Cin, D, H, W;  // x's own dimensions
+  int pad = 0;          // zero padding on every side (0: the valid convolution)
   const float* w;
   int Cout;
   const float* b;
@@ -27,9 +28,9 @@ struct Conv3dArgs {
   void* ws;
   size_t ws_bytes;
   cudaStream_t stream;
-  int OD() const { return D - 2; }
-  int OH() const { return H - 2; }
-  int OW() const { return W - 2; }
+  int OD() const { return D + 2 * pad - 2; }
+  int OH() const { return H + 2 * pad - 2; }
+  int OW() const { return W + 2 * pad - 2; }
 };
 
 struct DwsepArgs {
@@ -67,6 +68,15 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // conv3d_fused_select_path without touching ig3_last_error() (for size queries).
 int conv3d_select_quiet(int N, int Cin, int D, int H, int W, int Cout, int epi, int path);
+
+// The zero-padded (pad >= 0) stride-1 conv3d: argument checks, path choice on the
+// padded volume, workspace check and launch (conv3d_fused, conv3d_fused_pad).
+// `who` names the entry point in error messages.
+int conv3d_run(const float* x, int N, int Cin, int D, int H, int W, int pad, const float* w, int Cout,
+               const float* b, int epilogue, const ig3_epi_params* params, float* y, void* workspace,
+               size_t workspace_bytes, int path, void* stream, const char* who);
+// Workspace bytes conv3d_run needs (0 if none, or if the arguments are invalid).
+size_t conv3d_workspace(int N, int Cin, int D, int H, int W, int pad, int Cout, int epi, int path);
 
 // ---- FMA path (conv3d_fma.cu)
 size_t conv3d_fma_workspace(const Conv3dArgs& a);

@@ -114,12 +114,12 @@ int conv3d_fused(const float* x, int N, int Cin, int D, int H, int W,
  *
  * Arguments are those of conv3d_fused plus pad (0..16; 0 is conv3d_fused itself),
  * with every output size read as D+2*pad-2 etc. (POOL_REDUCE pools that grid).  The
- * library writes the zero-bordered copy [N][Cin][D+2*pad][H+2*pad][W+2*pad] of x at
- * the start of the workspace and runs conv3d_fused on it, so the workspace holds that
- * copy too: conv3d_fused_pad_workspace_size bytes (never 0 when pad > 0), 256-byte
- * aligned.  The path (and its requirements) is the one conv3d_fused takes for the
- * padded dimensions.  Requires D, H, W >= 1 and the padded copy below 2^31 elements;
- * there is no no-allocation variant.
+ * zero border is never written to memory: the kernels read x at the shifted
+ * coordinates and use zeros outside it.  The path (and its requirements) is the one
+ * conv3d_fused takes for the padded dimensions D+2*pad, H+2*pad, W+2*pad, and so is
+ * the workspace: conv3d_fused_pad_workspace_size bytes (0 when none is needed),
+ * 256-byte aligned.  Requires D, H, W >= 1 and the padded volume below 2^31
+ * elements; there is no no-allocation variant.
  */
 size_t conv3d_fused_pad_workspace_size(int N, int Cin, int D, int H, int W, int pad, int Cout,
                                        int epilogue, int path);

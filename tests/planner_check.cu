@@ -10,8 +10,9 @@
 using namespace ig3; using namespace ig3::tc;
 static int fails = 0;
 #define CHECK(c, ...) do { if (!(c)) { if (fails++ < 20) { printf("FAIL %s: ", #c); printf(__VA_ARGS__); printf("\n"); } } } while (0)
-void check(int N, int Cin, int D, int H, int W, int Cout, int epi, int sms, bool verbose) {
-  Plan pl = make_plan(N, Cin, D, H, W, Cout, epi, sms);
+void check(int N, int Cin, int D, int H, int W, int Cout, int epi, int sms, bool verbose, int flags = 0) {
+  Plan pl = make_plan(N, Cin, D, H, W, Cout, epi, sms, flags);
+  if (flags & kNoKwWindow) CHECK(!pl.ok || pl.prm.KDM != 9, "kd x kw window in a padded plan");
   if (!pl.ok) { if (verbose) printf("NO plan %d %d %d %d %d %d epi%d: %s\n", N, Cin, D, H, W, Cout, epi, pl.why); return; }
   TcParams p = pl.prm;
   if (verbose) printf("N%d Cin%d D%d H%d W%d Cout%d epi%d: KDM=%d HL=%d T=%d KSS=%d KS=%d nch=%d res=%d SB=%d NSLOT=%d S=%d P=%d units=%d NPOS=%d XS=%d smem=%zu\n",
@@ -125,6 +126,18 @@ int main() {
     for (int sms : {152, 148, 132, 7, 1})
       for (int epi : {s[6]})
         check(s[0],s[1],s[2],s[3],s[4],s[5],epi,sms, sms == 152);
+  // zero padding on chip: the virtual volumes (pitch W + roundup(pad + 2, 4) or W + 2 * pad) without the
+  // kd x kw window
+  int padded[][8] = {{16, 32, 32, 64, 64, 64, 1, 1}, {1, 16, 5, 7, 60, 16, 2, 1}, {1, 8, 4, 6, 32, 96, 3, 1},
+                     {1, 8, 5, 5, 16, 32, 4, 1}, {1, 8, 4, 5, 8, 48, 5, 1}, {2, 12, 5, 6, 13, 64, 1, 1},
+                     {2, 8, 7, 6, 28, 32, 2, 2}, {1, 8, 6, 9, 30, 16, 1, 2}, {2, 32, 6, 10, 64, 64, 1, 1}};
+  for (auto& s : padded)
+    for (int sms : {152, 148, 7}) {
+      const int P = s[6];
+      check(s[0], s[1], s[2] + 2 * P, s[3] + 2 * P, s[4] + 2 * P, s[5], s[7], sms, sms == 152, kNoKwWindow);
+      if (s[4] % 4 == 0 && P <= 4 && s[7] != 2)
+        check(s[0], s[1], s[2] + 2 * P, s[3] + 2 * P, s[4] + (P + 5) / 4 * 4, s[5], s[7], sms, sms == 152, kNoKwWindow);
+    }
   // random sweep
   srand(1);
   for (int i = 0; i < 3000; ++i) {

@@ -195,20 +195,22 @@ def test_conv3d_pad_argument_errors(lib):
     assert f(FAKE, 2048, 64, 62, 62, 62, 1, FAKE, 1, None, 1, None, FAKE, FAKE, 1 << 20, 2, None) == -1
     # the TC path's own requirements apply to the padded shape (Cout = 2)
     assert f(FAKE, 1, 1, 3, 3, 3, 1, FAKE, 2, None, 1, None, FAKE, FAKE, 1 << 20, 1, None) == -2
-    # a single voxel with pad 1 is a valid 1x1x1 output; it needs the bordered copy
-    need = q(1, 1, 1, 1, 1, 1, 1, 1, 2)
-    assert need >= 27 * 4 and need % 256 == 0
-    assert f(FAKE, 1, 1, 1, 1, 1, 1, FAKE, 1, None, 1, None, FAKE, None, 0, 2, None) == -5
-    assert f(FAKE, 1, 1, 1, 1, 1, 1, FAKE, 1, None, 1, None, FAKE, FAKE, need - 1, 2, None) == -5
-    assert f(FAKE, 1, 1, 1, 1, 1, 1, FAKE, 1, None, 1, None, FAKE, FAKE + 4, need, 2, None) == -5
+    # the border is never materialised: a padded call needs only the valid path's workspace
+    need = q(1, 16, 4, 5, 6, 1, 16, 1, 1)        # tensor cores: the split weights
+    assert need > 0 and need % 256 == 0
+    assert need <= lib.conv3d_fused_workspace_size(1, 16, 6, 7, 8, 16, 1, 1) + 256 * 1024
+    assert f(FAKE, 1, 16, 4, 5, 6, 1, FAKE, 16, None, 1, None, FAKE, None, 0, 1, None) == -5
+    assert f(FAKE, 1, 16, 4, 5, 6, 1, FAKE, 16, None, 1, None, FAKE, FAKE, need - 1, 1, None) == -5
+    assert f(FAKE, 1, 16, 4, 5, 6, 1, FAKE, 16, None, 1, None, FAKE, FAKE + 4, need, 1, None) == -5
+    assert q(1, 1, 1, 1, 1, 1, 1, 1, 2) == 0   # FMA path, tanh(mish): no workspace at all
+    # the padded conv3d + tanh(mish) workload: a few hundred KB of split weights, where the
+    # zero-bordered copy of x alone would be 303 MB
+    lib.conv3d_fused_workspace_size.restype = ctypes.c_size_t
+    assert 0 < q(16, 32, 32, 64, 64, 1, 64, 1, 1) < (1 << 20)
     # queries: zero for rejected arguments; pad 0 is the valid-conv query
     assert q(1, 1, 3, 3, 3, -1, 1, 1, 2) == 0
     assert q(0, 1, 3, 3, 3, 1, 1, 1, 2) == 0
-    lib.conv3d_fused_workspace_size.restype = ctypes.c_size_t
     assert q(1, 1, 4, 4, 4, 0, 1, 2, 2) == lib.conv3d_fused_workspace_size(1, 1, 4, 4, 4, 1, 2, 2)
-    # pad 1: the bordered copy [1][2][6][7][8] (256-byte aligned) plus the valid query of that shape
-    assert q(1, 2, 4, 5, 6, 1, 16, 1, 1) == \
-        (2 * 6 * 7 * 8 * 4 + 255) // 256 * 256 + lib.conv3d_fused_workspace_size(1, 2, 6, 7, 8, 16, 1, 1)
 
 
 def test_dwsep_auto_path_follows_measured_crossover(lib):

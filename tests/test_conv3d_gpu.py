@@ -301,6 +301,14 @@ PAD_CASES = [
     (1, 4, 3, 3, 3, 16, 2),     # pad 2, a 3x3x3 input
     (1, 3, 2, 3, 4, 5, 1),      # D = 2 input (valid conv impossible), odd channels: FMA
     (2, 5, 1, 1, 1, 16, 1),     # single voxel: one output per channel
+    # the border filled on chip: W % 4 == 0 gives aligned 16-byte loads over a virtual
+    # row pitch of W + 4 (pad <= 4), other widths scalar loads over W + 2*pad
+    (2, 32, 6, 10, 64, 64, 1),  # pitch 68, kd window (the padded workload's variant)
+    (1, 16, 5, 7, 60, 16, 2),   # pitch 64: Cout 16 kd x kw window
+    (1, 8, 4, 6, 32, 96, 3),    # pitch 36, one MMA per kd
+    (1, 8, 5, 5, 16, 32, 4),    # pitch 20, pad 4: the whole left border is the virtual row's first quad
+    (1, 8, 4, 5, 8, 48, 5),     # pad 5: scalar loads over pitch 18
+    (2, 12, 5, 6, 13, 64, 1),   # W % 4 != 0: scalar loads over pitch 15
 ]
 
 
@@ -322,7 +330,8 @@ def test_conv3d_pad_small_all_outputs(ig3, case, epi):
         assert_close(got.cpu().numpy(), ref, f"{case} {epi} {path}")
 
 
-@pytest.mark.parametrize("case", [(2, 8, 6, 8, 62, 16, 1), (1, 4, 5, 5, 5, 16, 1)],
+@pytest.mark.parametrize("case", [(2, 8, 6, 8, 62, 16, 1), (1, 4, 5, 5, 5, 16, 1), (2, 8, 7, 6, 28, 32, 2),
+                                  (1, 8, 6, 9, 30, 16, 1)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_conv3d_pad_pool_reduce(ig3, case):
     *shape, pad = case
@@ -337,6 +346,21 @@ def test_conv3d_pad_pool_reduce(ig3, case):
                                params={"divisor": 2.0, "pool": 2, "bias2": to_dev(t["bias2"])}, path=path, pad=pad)
         assert ig3.ig3_last_device_status() == 0
         assert_close(got.cpu().numpy(), ref, f"{case} pool {path}")
+
+
+def test_conv3d_pad_misaligned_input(ig3):
+    # x one float past a 16-byte boundary: the padded tensor-core path loads it with
+    # scalar loads over a virtual pitch of W + 2*pad.
+    wl = si.conv3d_workload("t", 1, 16, 5, 8, 64, 64, seed=3190, epilogue="tanh_mish", pad=1)
+    t = wl.generate_all()
+    ref = oracle.tanh_mish(oracle.conv3d_pad(t["x"], t["w"], t["b"], 1))
+    xs = torch.zeros(t["x"].size + 1, device="cuda")
+    xs[1:] = to_dev(t["x"]).reshape(-1)
+    x = xs[1:].view(t["x"].shape)
+    assert x.data_ptr() % 16 != 0
+    got = ig3.conv3d_fused(x, to_dev(t["w"]), to_dev(t["b"]), epilogue="tanh_mish", path="tc", pad=1)
+    assert ig3.ig3_last_device_status() == 0
+    assert_close(got.cpu().numpy(), ref, "padded, misaligned x, tc")
 
 
 def test_conv3d_pad_full_size_sampled(ig3):
