@@ -291,6 +291,88 @@ static __device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, floa
   asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
+// The convert of one A stage over the virtual padded volume (zero padding on chip):
+// the same items as the unpadded loops, with each position's source looked up in the
+// real input (padded_src) and zeros for the border.  Out of line, so that the
+// unpadded loops compile as they would without it.
+template <int KSS>
+static __device__ __noinline__ void convert_padded(const TcParams& p, int n, int d, int p0, int c0, int ct,
+                                                   uint32_t hi_base, uint32_t lo_base) {
+  constexpr int CC = KSS * 8;
+  const size_t cstride = (size_t)p.Dr * p.Hr * p.Wr;
+  if (p.vec) {
+    // A quad of virtual positions is wholly inside x's row or wholly in the zero
+    // border (the pitch and the first column are multiples of 4).
+    const int quads = p.NPOS >> 2;
+    const int vitems = (CC / 4) * quads;
+    for (int i0 = ct; i0 < vitems; i0 += 2 * kConvThreads) {
+      float4 v[2][4];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int i = i0 + k * kConvThreads;
+        const int grp = i / quads, qd = i - grp * quads;
+        const float* src = padded_src(p, n, d, p0 + 4 * qd);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int c = c0 + grp * 4 + j;
+          v[k][j] = (i < vitems && src != nullptr && c < p.Cin)
+                        ? __ldg(reinterpret_cast<const float4*>(src + (size_t)c * cstride))
+                        : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int i = i0 + k * kConvThreads;
+        if (i < vitems) {
+          const int grp = i / quads, qd = i - grp * quads;
+          const uint32_t off = (uint32_t)(grp * p.NPOS + 4 * qd) * 16u;
+          float h[4][4], l[4][4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            split_tf32(v[k][j].x, h[0][j], l[0][j]);
+            split_tf32(v[k][j].y, h[1][j], l[1][j]);
+            split_tf32(v[k][j].z, h[2][j], l[2][j]);
+            split_tf32(v[k][j].w, h[3][j], l[3][j]);
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            st_shared_v4(hi_base + off + 16u * e, h[e][0], h[e][1], h[e][2], h[e][3]);
+            st_shared_v4(lo_base + off + 16u * e, l[e][0], l[e][1], l[e][2], l[e][3]);
+          }
+        }
+      }
+    }
+  } else {
+    const int items = (CC / 4) * p.NPOS;
+    for (int i0 = ct; i0 < items; i0 += 2 * kConvThreads) {
+      float v[2][4];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int i = i0 + k * kConvThreads;
+        const int grp = i / p.NPOS, pp = i - grp * p.NPOS;
+        const float* src = padded_src(p, n, d, p0 + pp);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int c = c0 + grp * 4 + j;
+          v[k][j] = (i < items && src != nullptr && c < p.Cin) ? __ldg(src + (size_t)c * cstride) : 0.0f;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int i = i0 + k * kConvThreads;
+        if (i < items) {
+          const uint32_t off = (uint32_t)i * 16u;  // [group][position][4]
+          float h[4], l[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) split_tf32(v[k][j], h[j], l[j]);
+          st_shared_v4(hi_base + off, h[0], h[1], h[2], h[3]);
+          st_shared_v4(lo_base + off, l[0], l[1], l[2], l[3]);
+        }
+      }
+    }
+  }
+}
+
 template <int EPI, int KDM, int T, int KSS, bool RES, bool HL>
 __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -606,7 +688,9 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
             }
             mbar_arrive(&x_empty[rx.idx]);
             rx.next((uint32_t)p.XS);
-          } else if (p.vec && p.pad == 0) {
+          } else if (p.pad != 0) {
+            convert_padded<KSS>(p, un.n, d, p0, c0, ct, hi_base, lo_base);
+          } else if (p.vec) {
             // Item = (channel group, 4 consecutive positions): four 16-byte loads (one
             // per channel, coalesced along positions), transposed in registers to four
             // [position][4 channels] entries.  H*W % 4 == 0, so a quad lies wholly inside
@@ -650,52 +734,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
                 }
               }
             }
-          } else if (p.vec) {
-            // The same over the virtual padded volume: a quad of virtual positions is
-            // wholly inside x's row or wholly in the zero border (aligned quads).
-            const size_t cstride = (size_t)p.Dr * p.Hr * p.Wr;
-            const int quads = p.NPOS >> 2;
-            const int vitems = (CC / 4) * quads;
-            for (int i0 = ct; i0 < vitems; i0 += 2 * kConvThreads) {
-              float4 v[2][4];
-#pragma unroll
-              for (int k = 0; k < 2; ++k) {
-                const int i = i0 + k * kConvThreads;
-                const int grp = i / quads, qd = i - grp * quads;
-                const int pos = p0 + 4 * qd;
-                // The quad's source in the real input, or the zero border.
-                const float* src = padded_src(p, un.n, d, pos);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  const int c = c0 + grp * 4 + j;
-                  v[k][j] = (i < vitems && src != nullptr && c < p.Cin)
-                                ? __ldg(reinterpret_cast<const float4*>(src + (size_t)c * cstride))
-                                : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                }
-              }
-#pragma unroll
-              for (int k = 0; k < 2; ++k) {
-                const int i = i0 + k * kConvThreads;
-                if (i < vitems) {
-                  const int grp = i / quads, qd = i - grp * quads;
-                  const uint32_t off = (uint32_t)(grp * p.NPOS + 4 * qd) * 16u;
-                  float h[4][4], l[4][4];
-#pragma unroll
-                  for (int j = 0; j < 4; ++j) {
-                    split_tf32(v[k][j].x, h[0][j], l[0][j]);
-                    split_tf32(v[k][j].y, h[1][j], l[1][j]);
-                    split_tf32(v[k][j].z, h[2][j], l[2][j]);
-                    split_tf32(v[k][j].w, h[3][j], l[3][j]);
-                  }
-#pragma unroll
-                  for (int e = 0; e < 4; ++e) {
-                    st_shared_v4(hi_base + off + 16u * e, h[e][0], h[e][1], h[e][2], h[e][3]);
-                    st_shared_v4(lo_base + off + 16u * e, l[e][0], l[e][1], l[e][2], l[e][3]);
-                  }
-                }
-              }
-            }
-          } else if (p.pad == 0) {
+          } else
           for (int i0 = ct; i0 < items; i0 += 2 * kConvThreads) {
             float v[2][4];
 #pragma unroll
@@ -723,37 +762,6 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
                 st_shared_v4(lo_base + off, l[0], l[1], l[2], l[3]);
               }
             }
-          }
-          } else {
-          // Scalar loads over the virtual padded volume.
-          const size_t cstride = (size_t)p.Dr * p.Hr * p.Wr;
-          for (int i0 = ct; i0 < items; i0 += 2 * kConvThreads) {
-            float v[2][4];
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-              const int i = i0 + k * kConvThreads;
-              const int grp = i / p.NPOS, pp = i - grp * p.NPOS;
-              const int pos = p0 + pp;
-              const float* src = padded_src(p, un.n, d, pos);
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const int c = c0 + grp * 4 + j;
-                v[k][j] = (i < items && src != nullptr && c < p.Cin) ? __ldg(src + (size_t)c * cstride) : 0.0f;
-              }
-            }
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-              const int i = i0 + k * kConvThreads;
-              if (i < items) {
-                const uint32_t off = (uint32_t)i * 16u;  // [group][position][4]
-                float h[4], l[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) split_tf32(v[k][j], h[j], l[j]);
-                st_shared_v4(hi_base + off, h[0], h[1], h[2], h[3]);
-                st_shared_v4(lo_base + off, l[0], l[1], l[2], l[3]);
-              }
-            }
-          }
           }
           fence_proxy_async_smem();
           mbar_arrive(&a_full[ra.idx]);
