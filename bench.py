@@ -245,7 +245,11 @@ def make_call(ig3, wl, dev_t: dict, path: str):
             chosen = ig3.conv3d_fused_select_path(d["N"], d["Cin"], d["D"] + p2, d["H"] + p2, d["W"] + p2,
                                                   d["Cout"], wl.epilogue, path)
         else:
-            need, chosen = 0, "fma"   # strided: the FMA kernel, no workspace
+            # strided: the tensor-core kernel (its split weights in the workspace) where
+            # it applies, else the FMA kernel (no workspace)
+            need = ig3.conv3d_fused_ex_workspace_size(d["N"], d["Cin"], d["D"], d["H"], d["W"], wl.pad, wl.stride,
+                                                      d["Cout"], wl.epilogue, path)
+            chosen = "tc" if need > 0 else "fma"
         ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev_t["x"].device)
 
         def call():

@@ -167,6 +167,11 @@ def conv3d_fused_pad_workspace_size(N, Cin, D, H, W, pad, Cout, epilogue="tanh_m
                                                    _enum(EPILOGUES, epilogue, "epilogue"), _enum(PATHS, path, "path")))
 
 
+def conv3d_fused_ex_workspace_size(N, Cin, D, H, W, pad, stride, Cout, epilogue="tanh_mish", path="auto") -> int:
+    return int(lib.conv3d_fused_ex_workspace_size(N, Cin, D, H, W, pad, stride, Cout,
+                                                  _enum(EPILOGUES, epilogue, "epilogue"), _enum(PATHS, path, "path")))
+
+
 def conv3d_fused(x: torch.Tensor, w: torch.Tensor, b: torch.Tensor | None = None, epilogue="tanh_mish",
                  params: dict | None = None, out: torch.Tensor | None = None,
                  workspace: torch.Tensor | None = None, path="auto", stream=None, pad: int = 0,

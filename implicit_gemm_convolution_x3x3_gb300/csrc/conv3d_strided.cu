@@ -1,15 +1,17 @@
 // conv3d_fused_ex: the 3x3x3 convolution with zero padding P and stride S, fused
-// epilogue.  Stride 1 is conv3d_fused_pad (every path); stride 2 runs the FP32-FMA
-// kernel below.
+// epilogue.  Stride 1 is conv3d_fused_pad (every path); stride 2 runs the tensor-core
+// kernel of conv3d_strided_tc.cu where it applies, else the FP32-FMA kernel below.
 //
 // Definition ("Kimi-K2.6__l2_p47", the stride and padding discussion): the input
 // window of output od starts at od*S - P, reads outside the tensor are zero, and the
 // output size is (D + 2P - 3)/S + 1:
 //   conv[n,k,od,oh,ow] = b[k] + sum_{c,kd,kh,kw} w[k,c,kd,kh,kw] * x[n,c,od*S+kd-P,oh*S+kh-P,ow*S+kw-P].
 //
-// Stride 2 breaks the tensor-core kernel's addressing (the tap shift is a descriptor
-// offset into one tile of consecutive positions; strided positions are not), so it
-// runs on the FMA pipe: a CTA computes 16 x 32 outputs of one plane for 32 output
+// Stride 2 breaks the stride-1 tensor-core kernels' addressing (the tap shift is a
+// descriptor offset into one tile of consecutive positions; strided positions are
+// not); the strided tensor-core kernel gathers its A tiles instead and needs Cout a
+// multiple of 16 (<= 128), W a multiple of 4 and x 16-byte aligned.  Other shapes run
+// on the FMA pipe: a CTA computes 16 x 32 outputs of one plane for 32 output
 // channels, two rows per thread (64 accumulators).  Each input channel's strided halo,
 // 3 x ((16-1)S+3) x ((32-1)S+3), and its weights for the 32 outputs are staged in
 // shared memory by 4-byte cp.async copies whose zero-fill is the padding, two stages
@@ -151,6 +153,20 @@ __global__ void __launch_bounds__(kThreads) conv3d_strided_fma_kernel(
 // Output size of one dimension, or 0 if there is none.
 int out_dim(int s, int P, int S) { return s + 2 * P < 3 ? 0 : (s + 2 * P - 3) / S + 1; }
 
+// Which stride-2 path a call takes (IG3_PATH_TC or IG3_PATH_FMA), or a negative status.
+// Automatic choice: the tensor-core kernel wherever it applies (x alignment is checked
+// at the call).
+int strided_select(int N, int Cin, int D, int H, int W, int pad, int Cout, int epilogue, int path) {
+  using namespace ig3;
+  if (path != IG3_PATH_AUTO && path != IG3_PATH_FMA && path != IG3_PATH_TC)
+    return fail(IG3_ERR_INVALID_ARG, "conv3d_fused_ex: unknown path %d", path);
+  const char* why = conv3d_strided_tc_unsupported_reason(N, Cin, D, H, W, pad, Cout, epilogue);
+  const bool tc_ok = why[0] == '\0';
+  if (path == IG3_PATH_TC && !tc_ok) return fail(IG3_ERR_UNSUPPORTED, "conv3d_fused_ex: stride-2 tensor-core path: %s", why);
+  if (path == IG3_PATH_FMA) return IG3_PATH_FMA;
+  return tc_ok ? IG3_PATH_TC : IG3_PATH_FMA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -158,7 +174,12 @@ extern "C" {
 size_t conv3d_fused_ex_workspace_size(int N, int Cin, int D, int H, int W, int pad, int stride, int Cout,
                                       int epilogue, int path) {
   if (stride == 1) return conv3d_fused_pad_workspace_size(N, Cin, D, H, W, pad, Cout, epilogue, path);
-  return 0;  // stride 2 needs no workspace
+  if (stride != 2 || N < 1 || Cin < 1 || D < 1 || H < 1 || W < 1 || Cout < 1 || pad < 0 || pad > kMaxPad) return 0;
+  if (epilogue != IG3_EPI_NONE && epilogue != IG3_EPI_TANH_MISH) return 0;
+  if (path != IG3_PATH_AUTO && path != IG3_PATH_TC) return 0;
+  // The size query has no x pointer: it answers for a 16-byte aligned x.
+  if (ig3::conv3d_strided_tc_unsupported_reason(N, Cin, D, H, W, pad, Cout, epilogue)[0] != '\0') return 0;
+  return ig3::conv3d_strided_tc_workspace(Cin, Cout);
 }
 
 int conv3d_fused_ex(const float* x, int N, int Cin, int D, int H, int W, int pad, int stride, const float* w,
@@ -175,19 +196,30 @@ int conv3d_fused_ex(const float* x, int N, int Cin, int D, int H, int W, int pad
   if (epilogue != IG3_EPI_NONE && epilogue != IG3_EPI_TANH_MISH)
     return fail(epilogue == IG3_EPI_POOL_REDUCE ? IG3_ERR_UNSUPPORTED : IG3_ERR_INVALID_ARG,
                 "conv3d_fused_ex: stride 2 supports the NONE and TANH_MISH epilogues");
-  if (path != IG3_PATH_AUTO && path != IG3_PATH_FMA)
-    return fail(path == IG3_PATH_TC ? IG3_ERR_UNSUPPORTED : IG3_ERR_INVALID_ARG,
-                "conv3d_fused_ex: stride 2 runs on the FMA path only");
   const int OD = out_dim(D, pad, 2), OH = out_dim(H, pad, 2), OW = out_dim(W, pad, 2);
   if (OD < 1 || OH < 1 || OW < 1) return fail(IG3_ERR_UNSUPPORTED, "conv3d_fused_ex: no output for these sizes");
   const long long nx = (long long)N * Cin * D * H * W, ny = (long long)N * Cout * OD * OH * OW;
   if (nx >= (1ll << 31) || ny >= (1ll << 31) || (long long)Cout * Cin * 27 >= (1ll << 31))
     return fail(IG3_ERR_INVALID_ARG, "conv3d_fused_ex: a tensor has 2^31 or more elements");
+  int pth = strided_select(N, Cin, D, H, W, pad, Cout, epilogue, path);
+  if (pth < 0) return pth;
+  if (!x || !w || !y) return fail(IG3_ERR_INVALID_ARG, "conv3d_fused_ex: x, w and y must not be NULL");
+  if (pth == IG3_PATH_TC && reinterpret_cast<uintptr_t>(x) % 16 != 0) {
+    if (path == IG3_PATH_TC)
+      return fail(IG3_ERR_UNSUPPORTED, "conv3d_fused_ex: the stride-2 tensor-core path needs x 16-byte aligned");
+    pth = IG3_PATH_FMA;
+  }
+  if (pth == IG3_PATH_TC) {
+    Conv3dArgs a{};
+    a.x = x; a.N = N; a.Cin = Cin; a.D = D; a.H = H; a.W = W; a.pad = pad;
+    a.w = w; a.Cout = Cout; a.b = b; a.epi = epilogue; a.divisor = 1.0f; a.pool = 0; a.bias2 = nullptr;
+    a.y = y; a.ws = workspace; a.ws_bytes = workspace_bytes; a.stream = static_cast<cudaStream_t>(stream);
+    return conv3d_strided_tc_launch(a);
+  }
   const long long gz = (long long)N * ((Cout + kTCO - 1) / kTCO);
   const long long gx = (long long)((OW + kTW - 1) / kTW) * ((OH + kTH - 1) / kTH);
   if (gz > 65535 || OD > 65535 || gx >= (1ll << 31))
     return fail(IG3_ERR_UNSUPPORTED, "conv3d_fused_ex: grid too large for these sizes");
-  if (!x || !w || !y) return fail(IG3_ERR_INVALID_ARG, "conv3d_fused_ex: x, w and y must not be NULL");
   (void)params; (void)workspace; (void)workspace_bytes;
   const dim3 grid((unsigned)gx, (unsigned)OD, (unsigned)gz);
   const cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -94,6 +94,12 @@ bool conv3d_tc16_applies(const Conv3dArgs& a, const char** why);
 size_t conv3d_tc16_workspace(const Conv3dArgs& a);
 int conv3d_tc16_launch(const Conv3dArgs& a);
 
+// ---- stride-2 tensor-core path (conv3d_strided_tc.cu): A gathered into tensor memory.
+// Empty string if it handles this shape (x alignment aside), else the reason it does not.
+const char* conv3d_strided_tc_unsupported_reason(int N, int Cin, int D, int H, int W, int pad, int Cout, int epi);
+size_t conv3d_strided_tc_workspace(int Cin, int Cout);
+int conv3d_strided_tc_launch(const Conv3dArgs& a);
+
 // ---- depthwise-separable (dwsep.cu)
 const char* dwsep_tc_unsupported_reason(int N, int C, int H, int W, int Cout);
 int dwsep_fma_launch(const DwsepArgs& a);

@@ -138,10 +138,16 @@ int conv3d_fused_pad(const float* x, int N, int Cin, int D, int H, int W, int pa
  *                               * x[n,c,od*stride+kd-pad, oh*stride+kh-pad, ow*stride+kw-pad]
  *   y   [N][Cout][OD][OH][OW] with OD = (D + 2*pad - 3)/stride + 1 etc.
  * stride 1: exactly conv3d_fused_pad (every epilogue and path, its workspace).
- * stride 2: the FP32-FMA path only (IG3_PATH_AUTO or IG3_PATH_FMA; IG3_PATH_TC and the
- *           POOL_REDUCE epilogue return IG3_ERR_UNSUPPORTED), pad 0..16, no workspace
- *           (workspace may be NULL; the size query returns 0), and N * ceil(Cout/16)
- *           and OD at most 65535.
+ * stride 2: pad 0..16, the NONE and TANH_MISH epilogues (POOL_REDUCE returns
+ *           IG3_ERR_UNSUPPORTED).  IG3_PATH_TC (and IG3_PATH_AUTO wherever it applies)
+ *           runs a tensor-core kernel that gathers each tap's operand on chip; it needs
+ *           Cout a multiple of 16 and <= 128, W a multiple of 4, x 16-byte aligned and
+ *           ((W+2*pad-3)/2)*2 + 7 staged columns <= 256, and a 256-byte aligned
+ *           workspace of conv3d_fused_ex_workspace_size bytes (the split weights;
+ *           IG3_ERR_WORKSPACE if smaller).  The size query answers for a 16-byte
+ *           aligned x.  Otherwise AUTO and IG3_PATH_FMA run the FP32-FMA kernel (no
+ *           workspace; the size query returns 0 for IG3_PATH_FMA), which needs
+ *           N * ceil(Cout/32) and OD at most 65535.
  * Other strides return IG3_ERR_UNSUPPORTED.  Other arguments as conv3d_fused.
  */
 size_t conv3d_fused_ex_workspace_size(int N, int Cin, int D, int H, int W, int pad, int stride,

@@ -241,10 +241,15 @@ def test_conv3d_ex_argument_errors(lib):
     assert f(*args(5, 1, 0, 4, 1, 0)) == -2       # stride 0
     assert f(*args(5, -1, 2, 4, 1, 0)) == -1      # negative pad
     assert f(*args(5, 1, 2, 4, 2, 0)) == -2       # stride 2 with pool-reduce
-    assert f(*args(5, 1, 2, 16, 1, 1)) == -2      # stride 2 on the TC path
+    assert f(*args(5, 1, 2, 16, 1, 1)) == -2      # stride 2 on the TC path, W not a multiple of 4
+    assert f(*args(5, 1, 2, 8, 1, 1)) == -2       # stride 2 on the TC path, Cout not a multiple of 16
     assert f(*args(2, 0, 2, 4, 1, 0)) == -2       # no output (D + 2*pad < 3)
     assert f(*args(5, 1, 2, 4, 1, 0, None)) == -1  # NULL x
-    assert q(1, 2, 5, 5, 5, 1, 2, 4, 1, 0) == 0   # stride 2 needs no workspace
+    assert q(1, 2, 5, 5, 5, 1, 2, 4, 1, 0) == 0   # stride 2 on the FMA kernel needs no workspace
+    # stride 2 on tensor cores: the split weight blocks, 3 kd x K-steps x 576 * Cout bytes
+    assert q(1, 32, 32, 64, 64, 1, 2, 64, 1, 0) == 3 * 4 * 576 * 64
+    assert q(1, 32, 32, 64, 64, 1, 2, 64, 1, 2) == 0   # forced FMA
+    assert q(1, 32, 32, 64, 64, 1, 2, 64, 2, 0) == 0   # pool-reduce: not with stride 2
     assert q(1, 2, 5, 5, 5, 1, 1, 16, 1, 1) == lib.conv3d_fused_pad_workspace_size(1, 2, 5, 5, 5, 1, 16, 1, 1)
 
 

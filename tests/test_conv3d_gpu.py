@@ -385,7 +385,8 @@ def test_conv3d_pad_full_size_sampled(ig3):
 
 # ---------------------------------------------------------------- stride 2 (FMA path)
 # (N, Cin, D, H, W, Cout, pad): ragged tiles in every dim, Cout not a multiple of the
-# 16-channel block, odd and even input sizes, pad 0..2.
+# 16-channel block, odd and even input sizes, pad 0..2 (shapes the tensor-core kernel
+# does not take, so AUTO runs the FMA kernel too).
 STRIDE2_CASES = [
     (1, 3, 7, 9, 11, 5, 0),
     (2, 4, 8, 20, 70, 16, 1),
@@ -413,6 +414,62 @@ def test_conv3d_stride2_all_outputs(ig3, case, epi):
     got = ig3.conv3d_fused(to_dev(t["x"]), to_dev(t["w"]), None, epilogue=epi, pad=pad, stride=2)
     y0 = oracle.conv3d_ex(t["x"], t["w"], None, pad, 2)
     assert_close(got.cpu().numpy(), oracle.tanh_mish(y0) if epi == "tanh_mish" else y0, f"{case} no bias")
+
+
+# ---------------------------------------------------------------- stride 2 (tensor cores)
+# (N, Cin, D, H, W, Cout, pad): every tile shape of the gathering kernel (two tiles of
+# one kernel row per A stage for Cout <= 80, one tile of three rows for 96 and 112, one
+# of one row for 128), ragged position tiles, Cin not a multiple of 8, pad 0..3, and an
+# output plane whose whole window lies in the padding (bias only).
+STRIDE2_TC_CASES = [
+    (1, 3, 7, 9, 12, 16, 0),
+    (2, 8, 8, 20, 68, 32, 1),
+    (1, 5, 5, 6, 8, 48, 2),
+    (1, 12, 9, 33, 36, 64, 1),
+    (1, 8, 5, 8, 16, 96, 1),
+    (1, 40, 6, 12, 36, 128, 1),
+    (1, 8, 4, 4, 4, 16, 3),
+    (2, 24, 16, 64, 64, 64, 1),
+]
+
+
+@pytest.mark.parametrize("case", STRIDE2_TC_CASES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("epi", ["tanh_mish", "none"])
+def test_conv3d_stride2_tc_all_outputs(ig3, case, epi):
+    *shape, pad = case
+    N, Cin, D, H, W, Cout = shape
+    e = 1 if epi == "tanh_mish" else 0
+    assert ig3.lib.conv3d_fused_ex_workspace_size(N, Cin, D, H, W, pad, 2, Cout, e, 1) > 0  # the TC path applies
+    wl = si.conv3d_workload("t", N, Cin, D, H, W, Cout, seed=3300 + sum(case), epilogue=epi, pad=pad)
+    t = wl.generate_all()
+    y = oracle.conv3d_ex(t["x"], t["w"], t["b"], pad, 2)
+    ref = oracle.tanh_mish(y) if epi == "tanh_mish" else y
+    for path in ("tc", "auto"):
+        got = ig3.conv3d_fused(to_dev(t["x"]), to_dev(t["w"]), to_dev(t["b"]), epilogue=epi, path=path,
+                               pad=pad, stride=2)
+        assert ig3.ig3_last_device_status() == 0
+        assert tuple(got.shape) == ref.shape
+        assert_close(got.cpu().numpy(), ref, f"{case} {epi} {path}")
+    got = ig3.conv3d_fused(to_dev(t["x"]), to_dev(t["w"]), None, epilogue=epi, path="tc", pad=pad, stride=2)
+    y0 = oracle.conv3d_ex(t["x"], t["w"], None, pad, 2)
+    assert_close(got.cpu().numpy(), oracle.tanh_mish(y0) if epi == "tanh_mish" else y0, f"{case} no bias")
+
+
+def test_conv3d_stride2_tc_misaligned_x(ig3):
+    # x at a 4-byte offset: AUTO takes the FMA kernel, TC refuses (the tensor-map copy
+    # needs a 16-byte aligned base).
+    N, Cin, D, H, W, Cout, pad = 1, 8, 6, 8, 16, 32, 1
+    wl = si.conv3d_workload("t", N, Cin, D, H, W, Cout, seed=3390, epilogue="tanh_mish", pad=pad)
+    t = wl.generate_all()
+    flat = torch.zeros(t["x"].size + 1, dtype=torch.float32, device="cuda")
+    flat[1:] = to_dev(t["x"]).reshape(-1)
+    x = flat[1:].view(t["x"].shape)
+    assert x.data_ptr() % 16 != 0
+    ref = oracle.tanh_mish(oracle.conv3d_ex(t["x"], t["w"], t["b"], pad, 2))
+    got = ig3.conv3d_fused(x, to_dev(t["w"]), to_dev(t["b"]), epilogue="tanh_mish", pad=pad, stride=2)
+    assert_close(got.cpu().numpy(), ref, "misaligned x, auto")
+    with pytest.raises(RuntimeError):
+        ig3.conv3d_fused(x, to_dev(t["w"]), to_dev(t["b"]), epilogue="tanh_mish", path="tc", pad=pad, stride=2)
 
 
 def test_conv3d_stride2_full_size_sampled(ig3):

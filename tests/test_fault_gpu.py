@@ -70,6 +70,17 @@ def test_tensor_core_kernels_abort_and_recover(ig3):
             else:
                 ref = oracle.conv3d_tanh_mish(t["x"], t["w"], t["b"])
             assert_close(got.cpu().numpy(), ref, f"{name} after an aborted call")
+        wl = si.conv3d_workload("abort_s2", 2, 32, 16, 64, 64, 64, seed=4350, epilogue="tanh_mish", pad=1)
+        t = wl.generate_all()
+        dev = {k: to_dev(v) for k, v in t.items()}
+        ig3.ig3_set_wait_timeout_ns(1)
+        ig3.conv3d_fused(dev["x"], dev["w"], dev["b"], epilogue="tanh_mish", path="tc", pad=1, stride=2)
+        assert ig3.ig3_last_device_status() == -4, "stride 2"
+        ig3.ig3_set_wait_timeout_ns(0)
+        got = ig3.conv3d_fused(dev["x"], dev["w"], dev["b"], epilogue="tanh_mish", path="tc", pad=1, stride=2)
+        assert ig3.ig3_last_device_status() == 0
+        assert_close(got.cpu().numpy(), oracle.tanh_mish(oracle.conv3d_ex(t["x"], t["w"], t["b"], 1, 2)),
+                     "stride 2 after an aborted call")
         wl = si.dwsep_workload("abort_dwsep", 2, 32, 64, 128, 64, seed=4400)
         t = wl.generate_all()
         dev = {k: to_dev(v) for k, v in t.items()}

@@ -5,6 +5,8 @@ work unit of every CTA, recomputes the indices the kernel uses (TMEM columns, sl
 blocks, A rows, shared-memory offsets, input copies) against the plan's buffers;
 tests/tc16_plan_check.cu does the same for the 16-output-channel kernel with A in tensor
 memory (slot ring and its wrapped runs, A stages, B blocks, raw input copies, partials);
+tests/strided_tc_plan_check.cu does it for the stride-2 kernel (every gathered box
+element against the input coordinate of the definition, copies, columns, coverage);
 tests/dwsep_plan_check.cu does the same for the depthwise-separable planner (strips,
 shared-memory layout, TMEM ranges, tensor-map box and strides, row-copy coordinates).
 They need nvcc (host compilation only) but no GPU.
@@ -20,7 +22,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 
 
-@pytest.mark.parametrize("checker", ["planner_check.cu", "tc16_plan_check.cu", "dwsep_plan_check.cu"])
+@pytest.mark.parametrize("checker", ["planner_check.cu", "tc16_plan_check.cu", "strided_tc_plan_check.cu",
+                                     "dwsep_plan_check.cu"])
 def test_planner_index_bounds(checker):
     nvcc = shutil.which("nvcc") or ("/usr/local/cuda/bin/nvcc" if os.path.exists("/usr/local/cuda/bin/nvcc") else None)
     if nvcc is None:
