@@ -258,8 +258,7 @@ def make_call(ig3, wl, dev_t: dict, path: str):
         return call, out, chosen
     d = wl.dims
     out = torch.empty((d["N"], d["Cout"], d["H"], d["W"]), device=dev_t["x"].device)
-    # K != 3 runs on the FMA kernel only
-    chosen = ig3.dwsep_conv2d_select_path(d["N"], d["C"], d["H"], d["W"], d["Cout"], path) if d["K"] == 3 else "fma"
+    chosen = ig3.dwsep_conv2d_ex_select_path(d["N"], d["C"], d["H"], d["W"], d["K"], d["Cout"], path)
 
     def call():
         ig3.dwsep_conv2d(dev_t["x"], dev_t["w_dw"], dev_t["w_pw"], dev_t.get("b"), out=out, path=path)

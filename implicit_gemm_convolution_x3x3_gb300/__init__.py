@@ -24,6 +24,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "l
 __all__ = [
     "EPILOGUES", "PATHS", "Ig3Error", "lib", "conv3d_fused", "dwsep_conv2d",
     "conv3d_fused_workspace_size", "conv3d_fused_select_path", "dwsep_conv2d_select_path",
+    "dwsep_conv2d_ex_select_path",
     "conv3d_fused_noalloc", "NOALLOC_SCRATCH_BYTES",
     "ig3_status_string", "ig3_last_error", "ig3_last_device_status", "ig3_set_wait_timeout_ns",
     "ig3_selftest_bounded_wait", "ig3_kernel_launches", "ig3_version", "EXPORTED_SYMBOLS",
@@ -65,6 +66,7 @@ _SIGS = {
     "dwsep_conv2d_ex": (_i, [_p, _i, _i, _i, _i, _i, _p, _p, _i, _p, _p, _i, _p]),
     "conv3d_fused_select_path": (_i, [_i] * 8),
     "dwsep_conv2d_select_path": (_i, [_i] * 6),
+    "dwsep_conv2d_ex_select_path": (_i, [_i] * 7),
     "ig3_status_string": (ctypes.c_char_p, [_i]),
     "ig3_last_error": (ctypes.c_char_p, []),
     "ig3_last_device_status": (_i, [_p]),
@@ -146,6 +148,12 @@ def conv3d_fused_select_path(N, Cin, D, H, W, Cout, epilogue="tanh_mish", path="
 
 def dwsep_conv2d_select_path(N, C, H, W, Cout, path="auto") -> str:
     r = lib.dwsep_conv2d_select_path(N, C, H, W, Cout, _enum(PATHS, path, "path"))
+    _check(min(r, 0))
+    return PATH_NAMES[r]
+
+
+def dwsep_conv2d_ex_select_path(N, C, H, W, K, Cout, path="auto") -> str:
+    r = lib.dwsep_conv2d_ex_select_path(N, C, H, W, K, Cout, _enum(PATHS, path, "path"))
     _check(min(r, 0))
     return PATH_NAMES[r]
 

@@ -316,7 +316,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool first = true;
         for (int kd = un.kd_lo; ok && kd <= un.kd_hi; ++kd) {
           for (int ks = 0; ks < p.KS; ++ks) {
-            if (!(ok = wait_issue(&in_full[r.idx], r.phase, p.ctl, abort_flag))) break;
+            // No wait on in_full here: the producers waited for this stage's copies (the
+            // box and the weight block) before arriving on a_full, and this thread's wait
+            // on a_full below orders its MMAs after both (measured 3% faster than testing
+            // in_full too).
             const uint64_t b0 =
                 umma_desc_noswizzle(smem_addr(smem + (size_t)r.idx * p.stage_bytes + p.x_bytes), lbo, 128);
 #pragma unroll 1
@@ -512,9 +515,12 @@ int rows_spanned(int OH, int OW, int TP) {
 }
 
 // Tile shapes the kernel is instantiated for, in order of preference: (tiles per unit,
-// kernel rows per A stage).  Two tiles per unit halve the weight and halo traffic per
-// output; one kernel row per A stage keeps the A stages small enough for two of them.
-constexpr int kShapes[][2] = {{2, 1}, {1, 3}, {1, 1}};
+// kernel rows per A stage).  27 MMAs per A stage measured best (fewer hand-overs of the
+// issuing thread per MMA): two tiles of one kernel row per stage (18 MMAs, half the
+// weight and halo traffic per output) ran the stride-2 workload 7% slower, one tile of
+// one row 36% slower.  Where two A stages of three rows do not fit beside the
+// accumulators (Cout 128) the one-row stages take over.
+constexpr int kShapes[][2] = {{1, 3}, {1, 1}};
 
 Plan make_plan_uncached(int N, int Cin, int D, int H, int W, int P, int Cout, int epi, int sms) {
   Plan pl;
@@ -623,7 +629,6 @@ int launch(const Params& p, const CUtensorMap& xmap, size_t smem, int grid, cuda
 
 template <int EPI>
 int launch_epi(const Plan& pl, const Params& p, const CUtensorMap& xmap, int grid, cudaStream_t stream) {
-  if (pl.T == 2 && pl.KHG == 1) return launch<EPI, 2, 1>(p, xmap, pl.smem, grid, stream);
   if (pl.T == 1 && pl.KHG == 3) return launch<EPI, 1, 3>(p, xmap, pl.smem, grid, stream);
   if (pl.T == 1 && pl.KHG == 1) return launch<EPI, 1, 1>(p, xmap, pl.smem, grid, stream);
   return fail(IG3_ERR_UNSUPPORTED, "conv3d stride-2 TC: no kernel variant for %d tiles x %d rows", pl.T, pl.KHG);

@@ -45,15 +45,28 @@ namespace ig3 {
 namespace {
 
 constexpr int kMmaWarp = 0, kLoadWarp = 1;
-constexpr int kDwWarp0 = 2, kDwWarps = 8;    // two per TMEM lane quadrant
-constexpr int kEpiWarp0 = kDwWarp0 + kDwWarps, kEpiThreads = 128;
-constexpr int kThreads = 32 * kEpiWarp0 + kEpiThreads;
+constexpr int kDwWarp0 = 2, kEpiThreads = 128;
 constexpr int kTile = 128;      // pixels per tile
 constexpr int kHalo = 4;        // staged columns on each side (keeps the copy 16-byte aligned)
 constexpr int kBoxW = kTile + 2 * kHalo;
 constexpr int kRowSlots = 4;
 constexpr int kTmemCols = 512;
 constexpr int kACol0 = 256;     // first TMEM column of the A tiles
+
+// Role layout per depthwise size K.  K = 3: two depthwise warps per TMEM lane quadrant,
+// each holding two open output rows for up to 32 channels (64 partial sums); K = 5:
+// four per quadrant, four open rows for up to 16 channels (again 64 partial sums).
+template <int K>
+struct DwCfg {
+  static constexpr int P = (K - 1) / 2;                 // "same" padding
+  static constexpr int kPerQ = (K == 3) ? 2 : 4;        // depthwise warps per quadrant
+  static constexpr int kDwWarps = 4 * kPerQ;
+  static constexpr int kCMax = 64 / kPerQ;              // channels per depthwise warp, at most
+  static constexpr int kWRow = (K <= 4) ? 4 : 8;        // floats per kernel row of w_dw in smem
+  static constexpr int kEpiWarp0 = kDwWarp0 + kDwWarps;
+  static constexpr int kThreads = 32 * kEpiWarp0 + kEpiThreads;
+};
+static_assert(DwCfg<5>::P <= kHalo, "the staged halo must cover the depthwise window");
 
 struct DwParams {
   const float* w_dw;
@@ -128,8 +141,36 @@ __device__ __forceinline__ void tmem_st4(uint32_t taddr, float a, float b, float
                : "memory");
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// Kernel row kr of a K x K depthwise kernel (padded to kWRow floats, 16-byte aligned)
+// dotted with the K inputs of the window: init + sum over kw, folded from the last tap.
+template <int K, int kWRow>
+__device__ __forceinline__ float row_dot(const float* kr, const float (&xv)[K], float init, bool has_init) {
+  float k[K];
+#pragma unroll
+  for (int i = 0; i < K; i += 4) {
+    if (i + 4 <= kWRow && i + 1 < K) {
+      const float4 q4 = *reinterpret_cast<const float4*>(kr + i);
+      k[i] = q4.x;
+      if (i + 1 < K) k[i + 1] = q4.y;
+      if (i + 2 < K) k[i + 2] = q4.z;
+      if (i + 3 < K) k[i + 3] = q4.w;
+    } else {
+      k[i] = kr[i];
+    }
+  }
+  float v = has_init ? fmaf(k[K - 1], xv[K - 1], init) : k[K - 1] * xv[K - 1];
+#pragma unroll
+  for (int kw = K - 2; kw >= 0; --kw) v = fmaf(k[kw], xv[kw], v);
+  return v;
+}
+
+template <int K>
+__global__ void __launch_bounds__(DwCfg<K>::kThreads, 1)
     dwsep_tc_kernel(const DwParams p, const __grid_constant__ CUtensorMap xmap) {
+  using Cfg = DwCfg<K>;
+  constexpr int P = Cfg::P;
+  constexpr int kThreads = Cfg::kThreads, kDwWarps = Cfg::kDwWarps, kEpiWarp0 = Cfg::kEpiWarp0;
+  constexpr int kWRow = Cfg::kWRow, kCMax = Cfg::kCMax;
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
@@ -171,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   // Pointwise weights -> [K-step][k-half][2*Cout rows: hi, lo][4]; depthwise weights
-  // padded to [C][3 rows][4] so that one 16-byte load yields a row of the 3x3 kernel.
+  // padded to [C][K rows][kWRow] so that 16-byte loads yield a row of the K x K kernel.
   {
     const int total = (C >> 3) * 2 * (2 * Cout) * 4;
     float* sb = reinterpret_cast<float*>(smem_b);
@@ -188,9 +229,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       split_tf32(__ldg(&p.w_pw[(size_t)co * C + c]), hi, lo);
       sb[i] = (row < Cout) ? hi : lo;
     }
-    for (int i = tid; i < C * 12; i += kThreads) {
-      const int c = i / 12, r = (i % 12) >> 2, k = i & 3;
-      s_wdw[i] = (k < 3) ? __ldg(&p.w_dw[c * 9 + r * 3 + k]) : 0.0f;
+    for (int i = tid; i < C * K * kWRow; i += kThreads) {
+      const int c = i / (K * kWRow), r = (i / kWRow) % K, k = i % kWRow;
+      s_wdw[i] = (k < K) ? __ldg(&p.w_dw[(c * K + r) * K + k]) : 0.0f;
     }
     fence_proxy_async_smem();
   }
@@ -244,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int wb = (u / p.HR) % p.WB;
         const int n = u / (p.HR * p.WB);
         const int h0 = hr * p.R, h1 = min(p.H, h0 + p.R);
-        for (int r = h0 - 1; r <= h1; ++r) {
+        for (int r = h0 - P; r < h1 + P; ++r) {
           if (!wait_fast(&row_empty[rr.idx], rr.phase ^ 1u, p.ctl, abort_flag)) goto loader_done;
           mbar_arrive_expect_tx(&row_full[rr.idx], p.row_bytes);
           tma_load_3d(smem_rows + (size_t)rr.idx * p.row_bytes, &xmap, wb * kTile - kHalo, r, n * C, &row_full[rr.idx]);
@@ -271,24 +312,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < kEpiWarp0) {
     // ------------------------------------------------------------ depthwise
     const int q = warp & 3;                        // TMEM lane quadrant = pixels 32q .. 32q+31
-    const int half = (warp - kDwWarp0) >> 2;       // which half of the channels
+    const int grp = (warp - kDwWarp0) >> 2;        // which group of channels
     const int px = q * 32 + lane;
-    const int cper = C >> 1;                       // channels per warp (a multiple of 8, <= 32)
-    const int cbeg = half * cper;
+    const int cper = C / Cfg::kPerQ;               // channels per warp (a multiple of 4, <= kCMax)
+    const int cbeg = grp * cper;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     Ring ra;
     uint32_t rseq = 0;                             // rows consumed before this unit
     for (int u = blockIdx.x; u < p.units && !*abort_flag; u += gridDim.x) {
       const int hr = u % p.HR;
       const int h0 = hr * p.R, h1 = min(p.H, h0 + p.R);
-      // acc1[c]: output row r-1 so far (kernel rows 0, 1); acc2[c]: output row r (row 0).
-      float acc1[32], acc2[32];
+      // acc[t][c]: output row r - P + 1 + t so far (its kernel rows 0 .. K - 2 - t; the
+      // rows above the image are zeros).  Input row r completes output row r - P.
+      float acc[K - 1][kCMax];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) acc1[c] = acc2[c] = 0.0f;
-      for (int r = h0 - 1; r <= h1; ++r) {
-        const uint32_t sr = rseq + (uint32_t)(r - (h0 - 1));
+      for (int t = 0; t < K - 1; ++t)
+#pragma unroll
+        for (int c = 0; c < kCMax; ++c) acc[t][c] = 0.0f;
+      for (int r = h0 - P; r < h1 + P; ++r) {
+        const uint32_t sr = rseq + (uint32_t)(r - (h0 - P));
         if (!warp_wait(&row_full[sr % kRowSlots], (sr / kRowSlots) & 1u, p.ctl, abort_flag)) goto dw_done;
-        const bool emit = (r - 1 >= h0);           // output row r-1 completes with this row
+        const bool emit = (r - P >= h0);           // output row r - P completes with this row
         if (emit) {
           if (!warp_wait(&a_empty[ra.idx], ra.phase ^ 1u, p.ctl, abort_flag)) goto dw_done;
           tc_fence_after();
@@ -297,21 +341,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                            (size_t)cbeg * kBoxW + px + kHalo;
         const uint32_t a_hi = tmem_base + lane_off + (uint32_t)kACol0 + ra.idx * (uint32_t)(2 * C);
 #pragma unroll
-        for (int cg = 0; cg < 32; cg += 4) {
+        for (int cg = 0; cg < kCMax; cg += 4) {
           if (cg < cper) {
             float fin[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const int c = cg + j;
               const float* rw = row + c * kBoxW;
-              const float xl = rw[-1], xc = rw[0], xr = rw[1];
-              const float* kw = s_wdw + (cbeg + c) * 12;
-              const float4 k0 = *reinterpret_cast<const float4*>(kw);      // kernel row 0
-              const float4 k1 = *reinterpret_cast<const float4*>(kw + 4);  // kernel row 1
-              const float4 k2 = *reinterpret_cast<const float4*>(kw + 8);  // kernel row 2
-              fin[j] = fmaf(k2.x, xl, fmaf(k2.y, xc, fmaf(k2.z, xr, acc1[c])));
-              acc1[c] = fmaf(k1.x, xl, fmaf(k1.y, xc, fmaf(k1.z, xr, acc2[c])));
-              acc2[c] = fmaf(k0.x, xl, fmaf(k0.y, xc, k0.z * xr));
+              float xv[K];
+#pragma unroll
+              for (int kw = 0; kw < K; ++kw) xv[kw] = rw[kw - P];
+              const float* kp = s_wdw + (cbeg + c) * (K * kWRow);
+              // Kernel row K-1 closes the oldest open row; row kr feeds the row opened
+              // K-1-kr input rows ago; row 0 opens output row r + P.
+              fin[j] = row_dot<K, kWRow>(kp + (K - 1) * kWRow, xv, acc[0][c], true);
+#pragma unroll
+              for (int t = 0; t < K - 2; ++t)
+                acc[t][c] = row_dot<K, kWRow>(kp + (K - 2 - t) * kWRow, xv, acc[t + 1][c], true);
+              acc[K - 2][c] = row_dot<K, kWRow>(kp, xv, 0.0f, false);
             }
             if (emit) {
               float hi[4], lo[4];
@@ -333,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (emit) ra.next(2);
       }
-      rseq += (uint32_t)(h1 - h0 + 2);
+      rseq += (uint32_t)(h1 - h0 + 2 * P);
     }
   dw_done:;
   } else {
@@ -407,10 +454,16 @@ struct DwPlan {
   size_t smem = 0;
 };
 
-DwPlan make_dw_plan(int N, int C, int H, int W, int Cout, int sms = 148) {
+DwPlan make_dw_plan(int N, int C, int H, int W, int Cout, int K, int sms = 148) {
   DwPlan pl;
   DwParams& p = pl.prm;
   std::memset(&p, 0, sizeof(p));
+  if (K != 3 && K != 5) {
+    pl.why = "the tensor-core kernel takes depthwise sizes 3 and 5";
+    return pl;
+  }
+  const int P = (K - 1) / 2;
+  const int w_row = (K <= 4) ? 4 : 8;
   if (C % 16 != 0 || C > 64) {
     pl.why = "C must be a multiple of 16 and at most 64";
     return pl;
@@ -429,13 +482,13 @@ DwPlan make_dw_plan(int N, int C, int H, int W, int Cout, int sms = 148) {
   }
   p.N = N; p.C = C; p.H = H; p.W = W; p.Cout = Cout;
   p.WB = (W + kTile - 1) / kTile;
-  // Strips of R rows: each strip reads R + 2 rows, and the persistent grid takes
-  // ceil(units / SMs) rounds of strips; pick R minimising rounds x (R + 2).
+  // Strips of R rows: each strip reads R + 2P rows, and the persistent grid takes
+  // ceil(units / SMs) rounds of strips; pick R minimising rounds x (R + 2P).
   long long best = -1;
   for (int R : {8, 16, 32, 64}) {
     const int r = std::min(H, R);
     const long long u = (long long)N * p.WB * ((H + r - 1) / r);
-    const long long cost = (u + sms - 1) / sms * (r + 2);
+    const long long cost = (u + sms - 1) / sms * (r + 2 * P);
     if (best < 0 || cost < best) {
       best = cost;
       p.R = r;
@@ -452,7 +505,7 @@ DwPlan make_dw_plan(int N, int C, int H, int W, int Cout, int sms = 148) {
   p.row_bytes = (uint32_t)C * kBoxW * 4u;
   const uint32_t b_bytes = (uint32_t)(C / 8) * 2u * (2u * Cout) * 16u;
   p.off_wdw = b_bytes;
-  p.off_rows = (p.off_wdw + (uint32_t)C * 12u * 4u + 1023) / 1024 * 1024;
+  p.off_rows = (p.off_wdw + (uint32_t)(C * K * w_row) * 4u + 1023) / 1024 * 1024;
   p.off_bar = p.off_rows + kRowSlots * p.row_bytes;
   pl.smem = p.off_bar + 32 * 8;
   if (pl.smem + 2048 > (size_t)(227 * 1024)) {
@@ -466,9 +519,9 @@ DwPlan make_dw_plan(int N, int C, int H, int W, int Cout, int sms = 148) {
 
 }  // namespace
 
-const char* dwsep_tc_unsupported_reason(int N, int C, int H, int W, int Cout) {
+const char* dwsep_tc_unsupported_reason(int N, int C, int H, int W, int Cout, int K) {
   static thread_local char buf[160];
-  DwPlan pl = make_dw_plan(N, C, H, W, Cout);
+  DwPlan pl = make_dw_plan(N, C, H, W, Cout, K);
   if (pl.ok) return "";
   snprintf(buf, sizeof(buf), "%s", pl.why);
   return buf;
@@ -477,7 +530,7 @@ const char* dwsep_tc_unsupported_reason(int N, int C, int H, int W, int Cout) {
 int dwsep_tc_launch(const DwsepArgs& a) {
   const int sms = num_sms();
   if (sms <= 0) return fail(IG3_ERR_CUDA, "dwsep TC path: cannot query the SM count");
-  DwPlan pl = make_dw_plan(a.N, a.C, a.H, a.W, a.Cout, sms);
+  DwPlan pl = make_dw_plan(a.N, a.C, a.H, a.W, a.Cout, a.K, sms);
   if (!pl.ok) return fail(IG3_ERR_UNSUPPORTED, "dwsep TC path: %s", pl.why);
   if (reinterpret_cast<uintptr_t>(a.x) % 16 != 0)
     return fail(IG3_ERR_UNSUPPORTED, "dwsep TC path: x must be 16-byte aligned");
@@ -503,11 +556,14 @@ int dwsep_tc_launch(const DwsepArgs& a) {
                             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(IG3_ERR_CUDA, "dwsep TC path: tensor map encoding failed (%d)", (int)r);
 
-  cudaError_t e = cudaFuncSetAttribute(dwsep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
-  if (e != cudaSuccess) return cuda_status(e, "dwsep TC: set shared memory size");
   const int grid = std::min(p.units, sms);
-  dwsep_tc_kernel<<<grid, kThreads, pl.smem, a.stream>>>(p, xmap);
-  return count_launch(cuda_status(cudaGetLastError(), "dwsep TC kernel launch"));
+  auto go = [&](auto kernel, int threads) -> int {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+    if (e != cudaSuccess) return cuda_status(e, "dwsep TC: set shared memory size");
+    kernel<<<grid, threads, pl.smem, a.stream>>>(p, xmap);
+    return count_launch(cuda_status(cudaGetLastError(), "dwsep TC kernel launch"));
+  };
+  return a.K == 5 ? go(dwsep_tc_kernel<5>, DwCfg<5>::kThreads) : go(dwsep_tc_kernel<3>, DwCfg<3>::kThreads);
 }
 
 }  // namespace ig3

@@ -301,22 +301,44 @@ int dwsep_conv2d(const float* x, int N, int C, int H, int W, const float* w_dw, 
   return p == IG3_PATH_TC ? dwsep_tc_launch(a) : dwsep_fma_launch(a);
 }
 
+// Path of dwsep_conv2d_ex for K != 3 (IG3_PATH_TC or IG3_PATH_FMA), or a negative status.
+// K = 5 has a tensor-core kernel (the depthwise window on the FMA pipe, the pointwise
+// stage on tensor cores); AUTO takes it wherever it applies (x alignment is checked at
+// the call).  The 3x3 cost model does not apply to other K.
+int dwsep_ex_select(int N, int C, int H, int W, int K, int Cout, int path) {
+  if (K != 1 && K != 5 && K != 7)
+    return fail(IG3_ERR_UNSUPPORTED, "dwsep_conv2d_ex: depthwise size %d (1, 3, 5 or 7 are supported)", K);
+  if (path < IG3_PATH_AUTO || path > IG3_PATH_FMA)
+    return fail(IG3_ERR_INVALID_ARG, "dwsep_conv2d_ex: unknown path %d", path);
+  // The shape and element-count checks of the 3x3 entry point.
+  const int p0 = dwsep_select(N, C, H, W, Cout, IG3_PATH_FMA);
+  if (p0 < 0) return p0;
+  if ((long long)C * K * K >= (1ll << 31)) return fail(IG3_ERR_INVALID_ARG, "dwsep_conv2d_ex: w_dw too large");
+  const char* why = (K == 5) ? dwsep_tc_unsupported_reason(N, C, H, W, Cout, K) : "runs on the FMA path only";
+  const bool tc_ok = why[0] == '\0';
+  if (path == IG3_PATH_TC && !tc_ok)
+    return fail(IG3_ERR_UNSUPPORTED, "dwsep_conv2d_ex: depthwise size %d on the tensor-core path: %s", K, why);
+  return (path != IG3_PATH_FMA && tc_ok) ? IG3_PATH_TC : IG3_PATH_FMA;
+}
+
+int dwsep_conv2d_ex_select_path(int N, int C, int H, int W, int K, int Cout, int path) {
+  if (K == 3) return dwsep_select(N, C, H, W, Cout, path);
+  return dwsep_ex_select(N, C, H, W, K, Cout, path);
+}
+
 int dwsep_conv2d_ex(const float* x, int N, int C, int H, int W, int K, const float* w_dw, const float* w_pw, int Cout,
                     const float* b, float* y, int path, void* stream) {
   if (K == 3) return dwsep_conv2d(x, N, C, H, W, w_dw, w_pw, Cout, b, y, path, stream);
-  if (K != 1 && K != 5 && K != 7)
-    return fail(IG3_ERR_UNSUPPORTED, "dwsep_conv2d_ex: depthwise size %d (1, 3, 5 or 7 are supported)", K);
-  if (path == IG3_PATH_TC)
-    return fail(IG3_ERR_UNSUPPORTED, "dwsep_conv2d_ex: depthwise size %d runs on the FMA path only", K);
-  // The shape, path and element-count checks of the 3x3 entry point, on the FMA path.
-  const int p = dwsep_select(N, C, H, W, Cout, path == IG3_PATH_AUTO ? IG3_PATH_FMA : path);
-  if (p < 0) return p;
-  if ((long long)C * K * K >= (1ll << 31)) return fail(IG3_ERR_INVALID_ARG, "dwsep_conv2d_ex: w_dw too large");
+  const int sel = dwsep_ex_select(N, C, H, W, K, Cout, path);
+  if (sel < 0) return sel;
   if (!x || !w_dw || !w_pw || !y)
     return fail(IG3_ERR_INVALID_ARG, "dwsep_conv2d_ex: x, w_dw, w_pw and y must not be NULL");
   if (!current_device()) return fail(IG3_ERR_CUDA, "dwsep_conv2d_ex: device set-up failed");
   DwsepArgs a{x, N, C, H, W, w_dw, w_pw, Cout, b, y, static_cast<cudaStream_t>(stream)};
   a.K = K;
+  // A misaligned x goes to the FMA kernel when the caller left the choice to the library.
+  if (sel == IG3_PATH_TC && (path == IG3_PATH_TC || reinterpret_cast<uintptr_t>(x) % 16 == 0))
+    return dwsep_tc_launch(a);
   return dwsep_fma_launch(a);
 }
 

@@ -101,7 +101,8 @@ size_t conv3d_strided_tc_workspace(int Cin, int Cout);
 int conv3d_strided_tc_launch(const Conv3dArgs& a);
 
 // ---- depthwise-separable (dwsep.cu)
-const char* dwsep_tc_unsupported_reason(int N, int C, int H, int W, int Cout);
+// K: the depthwise size (3 or 5 on tensor cores).
+const char* dwsep_tc_unsupported_reason(int N, int C, int H, int W, int Cout, int K = 3);
 int dwsep_fma_launch(const DwsepArgs& a);
 int dwsep_tc_launch(const DwsepArgs& a);
 

@@ -216,8 +216,11 @@ int dwsep_conv2d(const float* x, int N, int C, int H, int W,
  *   dw[n,c,h,w] = sum_{kh,kw<K} w_dw[c,0,kh,kw] * x[n,c,h+kh-P,w+kw-P]   (zero outside)
  *   y[n,o,h,w]  = sum_c w_pw[o,c,0,0] * dw[n,c,h,w] + (b ? b[o] : 0)
  *   w_dw [C][1][K][K]; other arguments as dwsep_conv2d.
- * K = 3 takes every path of dwsep_conv2d; K = 1, 5, 7 run on the FP32-FMA path
- * (IG3_PATH_TC returns IG3_ERR_UNSUPPORTED); other K return IG3_ERR_UNSUPPORTED.
+ * K = 3 takes every path of dwsep_conv2d.  K = 5 has a tensor-core kernel too (the
+ * depthwise window on the FMA pipe, the pointwise stage on tensor cores, the depthwise
+ * result kept on chip) under the conditions of dwsep_conv2d's IG3_PATH_TC; IG3_PATH_AUTO
+ * takes it wherever they hold.  K = 1 and 7 run on the FP32-FMA path (IG3_PATH_TC
+ * returns IG3_ERR_UNSUPPORTED); other K return IG3_ERR_UNSUPPORTED.
  */
 int dwsep_conv2d_ex(const float* x, int N, int C, int H, int W, int K,
                     const float* w_dw, const float* w_pw, int Cout, const float* b,
@@ -227,6 +230,8 @@ int dwsep_conv2d_ex(const float* x, int N, int C, int H, int W, int K,
  * IG3_PATH_FMA), or a negative status if they would be rejected. */
 int conv3d_fused_select_path(int N, int Cin, int D, int H, int W, int Cout, int epilogue, int path);
 int dwsep_conv2d_select_path(int N, int C, int H, int W, int Cout, int path);
+/* The same for dwsep_conv2d_ex with a K x K depthwise stage. */
+int dwsep_conv2d_ex_select_path(int N, int C, int H, int W, int K, int Cout, int path);
 
 /* A static string naming a status code. */
 const char* ig3_status_string(int status);

@@ -2,8 +2,9 @@
 // the addresses its kernel and tensor map derive from a plan: strip length and unit
 // count, the shared-memory layout (row slots aligned for the tensor-map copies), the
 // TMEM column ranges, the tensor map's box and strides, and the x coordinate of every
-// row copy (a multiple of 16 bytes).  Shapes: a grid over the supported channel counts
-// and seeded random images, on several SM counts.  Prints the failures and "fails: N".
+// row copy (a multiple of 16 bytes), the rows a strip reads and the channels each
+// depthwise warp owns, for the 3x3 and 5x5 depthwise sizes.  Shapes: a grid over the
+// supported channel counts and seeded random images, on several SM counts.  Prints the failures and "fails: N".
 // Built by tests/test_planner_cpu.py (host code only).
 #include "../implicit_gemm_convolution_x3x3_gb300/csrc/dwsep_tc.cu"
 #include <cstdio>
@@ -12,8 +13,11 @@ using namespace ig3;
 static int fails = 0;
 #define CHECK(c, ...) do { if (!(c)) { if (fails++ < 20) { printf("FAIL %s: ", #c); printf(__VA_ARGS__); printf("\n"); } } } while (0)
 
-static void check(int N, int C, int H, int W, int Cout, int sms) {
-  DwPlan pl = make_dw_plan(N, C, H, W, Cout, sms);
+template <int K>
+static void check_k(int N, int C, int H, int W, int Cout, int sms) {
+  using Cfg = DwCfg<K>;
+  constexpr int P = Cfg::P;
+  DwPlan pl = make_dw_plan(N, C, H, W, Cout, K, sms);
   const bool supported = C % 16 == 0 && C <= 64 && Cout % 16 == 0 && Cout <= 128 && W % 4 == 0;
   CHECK(pl.ok == supported, "N%d C%d H%d W%d Cout%d: ok=%d (%s)", N, C, H, W, Cout, (int)pl.ok, pl.why);
   if (!pl.ok) return;
@@ -26,7 +30,12 @@ static void check(int N, int C, int H, int W, int Cout, int sms) {
   // shared memory
   const uint32_t b_bytes = (uint32_t)(C / 8) * 2u * (2u * Cout) * 16u;
   CHECK(p.off_wdw >= b_bytes, "B region");
-  CHECK(p.off_rows >= p.off_wdw + (uint32_t)C * 12u * 4u, "w_dw region");
+  CHECK(p.off_rows >= p.off_wdw + (uint32_t)(C * K * Cfg::kWRow) * 4u, "w_dw region");
+  CHECK(p.off_wdw % 16 == 0 && (K * Cfg::kWRow * 4) % 16 == 0 && Cfg::kWRow >= K, "w_dw rows 16-byte aligned");
+  // depthwise warps: kPerQ per quadrant, C / kPerQ channels each, groups of 4 (tcgen05.st x4)
+  CHECK(C % Cfg::kPerQ == 0 && (C / Cfg::kPerQ) % 4 == 0 && C / Cfg::kPerQ <= Cfg::kCMax, "channels per warp");
+  CHECK(Cfg::kThreads <= 1024 && Cfg::kEpiWarp0 + 4 == Cfg::kThreads / 32, "roles");
+  CHECK(P <= kHalo, "halo");
   CHECK(p.off_rows % 1024 == 0 && p.row_bytes % 16 == 0 && p.row_bytes == (uint32_t)C * kBoxW * 4u, "row slots");
   CHECK(p.off_bar >= p.off_rows + kRowSlots * p.row_bytes && p.off_bar % 8 == 0, "barriers");
   CHECK(pl.smem >= p.off_bar + 32 * 8 && pl.smem + 2048 <= (size_t)(227 * 1024), "smem %zu", pl.smem);
@@ -42,9 +51,18 @@ static void check(int N, int C, int H, int W, int Cout, int sms) {
     const int h0 = hr * p.R, h1 = std::min(p.H, h0 + p.R);
     const long long xcoord = (long long)wb * kTile - kHalo;
     CHECK((xcoord * 4) % 16 == 0, "x coordinate %lld", xcoord);
-    CHECK(h0 - 1 >= -1 && h1 <= H && h0 < h1, "rows");
+    CHECK(h0 - P >= -P && h1 + P - 1 <= H - 1 + P && h0 < h1, "rows");
+    // the depthwise warps consume rows h0-P .. h1+P-1 in the loader's order: R + 2P rows
+    CHECK((h1 + P) - (h0 - P) == (h1 - h0) + 2 * P, "rows per strip");
+    // pixels px - P .. px + P of the tile lie inside the staged row [w0 - kHalo, w0 + 128 + kHalo)
+    CHECK(kHalo - P >= 0 && kTile - 1 + kHalo + P < kBoxW, "staged columns");
     CHECK((long long)n * C + C <= (long long)N * C, "channel block");
   }
+}
+
+static void check(int N, int C, int H, int W, int Cout, int sms) {
+  check_k<3>(N, C, H, W, Cout, sms);
+  check_k<5>(N, C, H, W, Cout, sms);
 }
 
 int main() {

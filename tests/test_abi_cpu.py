@@ -260,7 +260,16 @@ def test_dwsep_ex_argument_errors(lib):
         [ctypes.c_void_p] * 2 + [ctypes.c_int, ctypes.c_void_p]
     assert f(FAKE, 1, 4, 5, 5, 4, FAKE, FAKE, 4, None, FAKE, 2, None) == -2   # K = 4
     assert f(FAKE, 1, 4, 5, 5, 9, FAKE, FAKE, 4, None, FAKE, 2, None) == -2   # K = 9
-    assert f(FAKE, 1, 16, 8, 8, 5, FAKE, FAKE, 16, None, FAKE, 1, None) == -2  # K = 5 on the TC path
+    assert f(FAKE, 1, 16, 8, 8, 7, FAKE, FAKE, 16, None, FAKE, 1, None) == -2  # K = 7 on the TC path
+    assert f(FAKE, 1, 24, 8, 8, 5, FAKE, FAKE, 16, None, FAKE, 1, None) == -2  # K = 5 on TC: C not a multiple of 16
+    sel = lib.dwsep_conv2d_ex_select_path
+    sel.restype = ctypes.c_int
+    TC, FMA = 1, 2
+    assert sel(16, 64, 512, 512, 5, 128, 0) == TC      # the 5x5 workload: tensor cores
+    assert sel(16, 64, 512, 512, 7, 128, 0) == FMA     # 7x7: FMA only
+    assert sel(1, 24, 8, 8, 5, 16, 0) == FMA           # C off the 16-channel blocks
+    assert sel(1, 16, 8, 8, 5, 16, 2) == FMA           # forced FMA
+    assert sel(1, 16, 8, 8, 4, 16, 0) == -2            # K = 4
     assert f(FAKE, 0, 4, 5, 5, 5, FAKE, FAKE, 4, None, FAKE, 0, None) == -1   # N = 0
     assert f(None, 1, 4, 5, 5, 7, FAKE, FAKE, 4, None, FAKE, 0, None) == -1   # NULL x
     assert f(FAKE, 70000, 64, 512, 512, 5, FAKE, FAKE, 4, None, FAKE, 2, None) == -1  # too many elements

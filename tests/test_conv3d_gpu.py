@@ -417,10 +417,10 @@ def test_conv3d_stride2_all_outputs(ig3, case, epi):
 
 
 # ---------------------------------------------------------------- stride 2 (tensor cores)
-# (N, Cin, D, H, W, Cout, pad): every tile shape of the gathering kernel (two tiles of
-# one kernel row per A stage for Cout <= 80, one tile of three rows for 96 and 112, one
-# of one row for 128), ragged position tiles, Cin not a multiple of 8, pad 0..3, and an
-# output plane whose whole window lies in the padding (bias only).
+# (N, Cin, D, H, W, Cout, pad): both A-stage shapes of the gathering kernel (three
+# kernel rows for Cout <= 112, one row for 128), ragged position tiles, Cin not a
+# multiple of 8, pad 0..3, and an output plane whose whole window lies in the padding
+# (bias only).
 STRIDE2_TC_CASES = [
     (1, 3, 7, 9, 12, 16, 0),
     (2, 8, 8, 20, 68, 32, 1),

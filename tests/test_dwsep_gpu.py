@@ -96,7 +96,8 @@ def test_dwsep_misaligned_input(ig3):
 
 
 # ---------------------------------------------------------------- K x K depthwise (FMA path)
-# (N, C, H, W, Cout, K): ragged tiles, channel counts off the 8 / 32 blocks, K = 1, 5, 7.
+# (N, C, H, W, Cout, K): ragged tiles, channel counts off the 8 / 32 blocks, K = 1, 5, 7
+# (shapes the tensor-core kernels do not take, so AUTO runs the FMA kernel too).
 K_CASES = [
     (1, 5, 9, 70, 33, 5),
     (2, 16, 5, 64, 32, 7),
@@ -117,6 +118,48 @@ def test_dwsep_k_all_outputs(ig3, case):
         assert_close(got.cpu().numpy(), ref, f"{case} {path}")
     with pytest.raises(ig3.Ig3Error):
         ig3.dwsep_conv2d(to_dev(t["x"]), to_dev(t["w_dw"]), to_dev(t["w_pw"]), None, path="tc")
+
+
+# ---------------------------------------------------------------- 5x5 depthwise (tensor cores)
+# (N, C, H, W, Cout, with_bias): ragged segments and strips, the full channel counts,
+# images smaller than the window (H = 1, 2: every halo row from outside the image).
+K5_TC_CASES = [
+    (2, 16, 9, 68, 32, False),
+    (1, 64, 6, 128, 128, True),
+    (1, 32, 5, 36, 48, True),
+    (1, 16, 1, 8, 16, False),
+    (1, 16, 2, 4, 16, True),
+    (2, 16, 37, 132, 16, False),
+    (1, 48, 70, 260, 112, True),
+]
+
+
+@pytest.mark.parametrize("case", K5_TC_CASES, ids=lambda c: "x".join(map(str, c[:5])) + ("b" if c[5] else ""))
+def test_dwsep_k5_tc_all_outputs(ig3, case):
+    N, C, H, W, Cout, wb = case
+    assert ig3.dwsep_conv2d_ex_select_path(N, C, H, W, 5, Cout, "auto") == "tc"
+    wl = si.dwsep_workload("t", N, C, H, W, Cout, seed=3500 + N + C + H + W + Cout, with_bias=wb, K=5)
+    t = wl.generate_all()
+    ref = oracle.dwsep_k(t["x"], t["w_dw"], t["w_pw"], t.get("b"))
+    for path in ("tc", "auto", "fma"):
+        assert_close(run(ig3, t, path), ref, f"{case} {path}")
+
+
+def test_dwsep_k5_misaligned_input(ig3):
+    N, C, H, W, Cout = 1, 32, 12, 64, 64
+    wl = si.dwsep_workload("t", N, C, H, W, Cout, seed=3590, with_bias=False, K=5)
+    t = wl.generate_all()
+    ref = oracle.dwsep_k(t["x"], t["w_dw"], t["w_pw"], None)
+    buf = torch.empty(t["x"].size + 1, dtype=torch.float32, device="cuda")
+    x = buf[1:].view(t["x"].shape)
+    x.copy_(torch.from_numpy(t["x"]))
+    assert x.data_ptr() % 16 != 0
+    w_dw = to_dev(t["w_dw"]); w_pw = to_dev(t["w_pw"])
+    with pytest.raises(ig3.Ig3Error):
+        ig3.dwsep_conv2d(x, w_dw, w_pw, None, path="tc")
+    out = ig3.dwsep_conv2d(x, w_dw, w_pw, None)
+    assert ig3.ig3_last_device_status() == 0
+    assert_close(out.cpu().numpy(), ref, "K=5 misaligned auto")
 
 
 def test_dwsep_k5_full_size_sampled(ig3):

@@ -91,6 +91,17 @@ def test_tensor_core_kernels_abort_and_recover(ig3):
         got = ig3.dwsep_conv2d(dev["x"], dev["w_dw"], dev["w_pw"], None, path="tc")
         assert ig3.ig3_last_device_status() == 0
         assert_close(got.cpu().numpy(), oracle.dwsep(t["x"], t["w_dw"], t["w_pw"], None), "dwsep after an aborted call")
+        wl = si.dwsep_workload("abort_dwsep5", 2, 32, 64, 128, 64, seed=4410, K=5)
+        t = wl.generate_all()
+        dev = {k: to_dev(v) for k, v in t.items()}
+        ig3.ig3_set_wait_timeout_ns(1)
+        ig3.dwsep_conv2d(dev["x"], dev["w_dw"], dev["w_pw"], None, path="tc")
+        assert ig3.ig3_last_device_status() == -4, "dwsep K=5"
+        ig3.ig3_set_wait_timeout_ns(0)
+        got = ig3.dwsep_conv2d(dev["x"], dev["w_dw"], dev["w_pw"], None, path="tc")
+        assert ig3.ig3_last_device_status() == 0
+        assert_close(got.cpu().numpy(), oracle.dwsep_k(t["x"], t["w_dw"], t["w_pw"], None),
+                     "dwsep K=5 after an aborted call")
     finally:
         ig3.ig3_set_wait_timeout_ns(0)
         ig3.ig3_last_device_status()
