@@ -45,7 +45,7 @@ namespace ig3 {
 namespace {
 
 constexpr int kMmaWarp = 0, kLoadWarp = 1;
-constexpr int kDwWarp0 = 2, kEpiThreads = 128;
+constexpr int kEpiThreads = 128;
 constexpr int kTile = 128;      // pixels per tile
 constexpr int kHalo = 4;        // staged columns on each side (keeps the copy 16-byte aligned)
 constexpr int kBoxW = kTile + 2 * kHalo;
@@ -53,17 +53,24 @@ constexpr int kRowSlots = 4;
 constexpr int kTmemCols = 512;
 constexpr int kACol0 = 256;     // first TMEM column of the A tiles
 
-// Role layout per depthwise size K.  K = 3: two depthwise warps per TMEM lane quadrant,
-// each holding two open output rows for up to 32 channels (64 partial sums); K = 5:
-// four per quadrant, four open rows for up to 16 channels (again 64 partial sums).
+// Role layout per depthwise size K.  K = 3: an MMA warp, a loader warp, two depthwise
+// warps per TMEM lane quadrant (each holding two open output rows for up to 32 channels:
+// 64 partial sums) and four epilogue warps.  K = 5: four depthwise warps per quadrant
+// (four open rows for up to 16 channels, again 64 partial sums) and four epilogue
+// warps, the first of which also runs the row loads and the MMA issue (kMerged): 20
+// warps, five per SM sub-partition, leave 96 registers per thread (22 would leave 80,
+// and the partial sums would spill).
 template <int K>
 struct DwCfg {
   static constexpr int P = (K - 1) / 2;                 // "same" padding
+  static constexpr bool kMerged = (K != 3);
   static constexpr int kPerQ = (K == 3) ? 2 : 4;        // depthwise warps per quadrant
   static constexpr int kDwWarps = 4 * kPerQ;
   static constexpr int kCMax = 64 / kPerQ;              // channels per depthwise warp, at most
   static constexpr int kWRow = (K <= 4) ? 4 : 8;        // floats per kernel row of w_dw in smem
+  static constexpr int kDwWarp0 = kMerged ? 0 : 2;
   static constexpr int kEpiWarp0 = kDwWarp0 + kDwWarps;
+  static constexpr int kOwnerWarp = kMerged ? kEpiWarp0 : kMmaWarp;  // allocates TMEM
   static constexpr int kThreads = 32 * kEpiWarp0 + kEpiThreads;
 };
 static_assert(DwCfg<5>::P <= kHalo, "the staged halo must cover the depthwise window");
@@ -164,12 +171,208 @@ __device__ __forceinline__ float row_dot(const float* kr, const float (&xv)[K], 
   return v;
 }
 
+// Row loads and MMA issue run by one thread as a state machine that never blocks
+// (K = 5: the first epilogue warp's lane 0 calls it while it waits for accumulators).
+struct CtlState {
+  int lu, ln, lwb, lr, lr1;  // loader: unit, image, segment, next input row, end row
+  bool lmore;
+  int mu, mh, mh1;           // MMA: unit, next output row, end row
+  bool mmore;
+  Ring rr, ra, rm;           // row slots, A tiles, accumulators
+  uint32_t issued;           // row copies issued
+};
+
+__device__ __forceinline__ void ctl_unit_rows(const DwParams& p, int u, int P, int& n, int& wb, int& r0, int& r1,
+                                              int& h0, int& h1) {
+  const int hr = u % p.HR;
+  wb = (u / p.HR) % p.WB;
+  n = u / (p.HR * p.WB);
+  h0 = hr * p.R;
+  h1 = min(p.H, h0 + p.R);
+  r0 = h0 - P;
+  r1 = h1 + P;
+}
+
+__device__ __forceinline__ void ctl_init(const DwParams& p, int P, CtlState& cs) {
+  cs = CtlState{};
+  cs.lu = cs.mu = blockIdx.x;
+  cs.lmore = cs.mmore = blockIdx.x < p.units;
+  if (cs.lmore) {
+    int h0, h1;
+    ctl_unit_rows(p, cs.lu, P, cs.ln, cs.lwb, cs.lr, cs.lr1, h0, h1);
+    cs.mh = h0;
+    cs.mh1 = h1;
+  }
+}
+
+// One round: as many row copies as there are free slots, and the MMAs of one output
+// row if its A tile and an accumulator are ready.
+__device__ __forceinline__ void ctl_progress(const DwParams& p, const CUtensorMap* xmap, int P, CtlState& cs,
+                                             uint8_t* smem_b, uint8_t* smem_rows, uint64_t* row_full,
+                                             uint64_t* row_empty, uint64_t* a_full, uint64_t* a_empty,
+                                             uint64_t* acc_full, uint64_t* acc_empty, uint32_t tmem_base) {
+  for (int k = 0; k < kRowSlots && cs.lmore; ++k) {
+    if (!test_wait(&row_empty[cs.rr.idx], cs.rr.phase ^ 1u)) break;
+    mbar_arrive_expect_tx(&row_full[cs.rr.idx], p.row_bytes);
+    tma_load_3d(smem_rows + (size_t)cs.rr.idx * p.row_bytes, xmap, cs.lwb * kTile - kHalo, cs.lr, cs.ln * p.C,
+                &row_full[cs.rr.idx]);
+    cs.rr.next(kRowSlots);
+    ++cs.issued;
+    if (++cs.lr == cs.lr1) {
+      cs.lu += gridDim.x;
+      cs.lmore = cs.lu < p.units;
+      if (cs.lmore) {
+        int h0, h1;
+        ctl_unit_rows(p, cs.lu, P, cs.ln, cs.lwb, cs.lr, cs.lr1, h0, h1);
+      }
+    }
+  }
+  if (cs.mmore && test_wait(&a_full[cs.ra.idx], cs.ra.phase) && test_wait(&acc_empty[cs.rm.idx], cs.rm.phase ^ 1u)) {
+    tc_fence_after();
+    const int Cout = p.Cout;
+    const uint32_t idesc = umma_idesc_tf32(128, Cout);
+    const uint64_t b_desc0 = umma_desc_noswizzle(smem_addr(smem_b), (uint32_t)(2 * Cout) * 16u, 128);
+    const uint32_t ks_b_u = (uint32_t)(4 * Cout);
+    const uint32_t lo_u = (uint32_t)Cout;
+    const uint32_t a_hi = tmem_base + (uint32_t)kACol0 + cs.ra.idx * (uint32_t)(2 * p.C);
+    const uint32_t a_lo = a_hi + (uint32_t)p.C;
+    const uint32_t d = tmem_base + cs.rm.idx * (uint32_t)Cout;
+    for (int ks = 0; ks < (p.C >> 3); ++ks) {
+      const uint64_t bh = b_desc0 + (uint64_t)((uint32_t)ks * ks_b_u);
+      umma_tf32_ts(d, a_hi + 8u * ks, bh, idesc, ks > 0 ? 1u : 0u);
+      umma_tf32_ts(d, a_hi + 8u * ks, bh + lo_u, idesc, 1u);
+      umma_tf32_ts(d, a_lo + 8u * ks, bh, idesc, 1u);
+    }
+    umma_commit(&a_empty[cs.ra.idx]);
+    umma_commit(&acc_full[cs.rm.idx]);
+    cs.ra.next(2);
+    cs.rm.next(2);
+    if (++cs.mh == cs.mh1) {
+      cs.mu += gridDim.x;
+      cs.mmore = cs.mu < p.units;
+      if (cs.mmore) {
+        int n, wb, r0, r1;
+        ctl_unit_rows(p, cs.mu, P, n, wb, r0, r1, cs.mh, cs.mh1);
+      }
+    }
+  }
+}
+
+// Epilogue warps of the merged layout: each drains its TMEM lane quadrant of every
+// output row (16-column chunks, the next load in flight while one is stored); while a
+// warp waits for an accumulator, the first one also runs ctl_progress.  Every wait is
+// bounded by the time limit; on a timeout or an abort the control thread lets its
+// copies in flight land and waits for its MMAs before the CTA exits.
+template <class Cfg>
+__device__ __forceinline__ void merged_epilogue(const DwParams& p, const CUtensorMap& xmap, uint8_t* smem_b,
+                                                uint8_t* smem_rows, uint64_t* row_full, uint64_t* row_empty,
+                                                uint64_t* a_full, uint64_t* a_empty, uint64_t* acc_full,
+                                                uint64_t* acc_empty, uint64_t* mma_done, uint32_t tmem_base,
+                                                volatile int* abort_flag, int warp, int lane) {
+  constexpr int P = Cfg::P;
+  const bool ctl = (warp == Cfg::kEpiWarp0);
+  const int q = warp & 3;
+  const int px = q * 32 + lane;
+  const int HW = p.H * p.W;
+  const int Cout = p.Cout;
+  CtlState cs;
+  if (ctl && lane == 0) ctl_init(p, P, cs);
+  Ring racc;
+  bool ok = true;
+  for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+    const int hr = u % p.HR;
+    const int wb = (u / p.HR) % p.WB;
+    const int n = u / (p.HR * p.WB);
+    const int w = wb * kTile + px;
+    const int h0 = hr * p.R, h1 = min(p.H, h0 + p.R);
+    for (int h = h0; h < h1; ++h) {
+      // Wait for the accumulator (the control thread keeps the pipeline moving).
+      uint64_t t0 = 0;
+      if (lane == 0) t0 = globaltimer_ns();
+      for (uint32_t it = 0;; ++it) {
+        if (ctl) {
+          if (lane == 0)
+            ctl_progress(p, &xmap, P, cs, smem_b, smem_rows, row_full, row_empty, a_full, a_empty, acc_full,
+                         acc_empty, tmem_base);
+          __syncwarp();
+        }
+        uint32_t st = 0;  // 1: ready, 2: give up
+        if (lane == 0) {
+          if (test_wait(&acc_full[racc.idx], racc.phase)) {
+            st = 1;
+          } else if (*abort_flag) {
+            st = 2;
+          } else if ((it & 15u) == 15u && globaltimer_ns() - t0 > p.ctl.limit_ns) {
+            *abort_flag = 1;
+            atomicOr(p.ctl.status, kDevStatusTimeout);
+            st = 2;
+          }
+        }
+        st = __shfl_sync(0xffffffffu, st, 0);
+        if (st == 1) break;
+        if (st == 2) {
+          ok = false;
+          break;
+        }
+      }
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + racc.idx * (uint32_t)Cout;
+      float* yb = p.y + (size_t)n * Cout * HW + (size_t)h * p.W + w;
+      float va[16], vb[16];
+      tmem_ld16(tb, va);
+      tmem_wait_ld();
+      for (int c0 = 0; c0 < Cout; c0 += 32) {
+        if (c0 + 16 < Cout) tmem_ld16(tb + (uint32_t)(c0 + 16), vb);
+        if (w < p.W) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) yb[(size_t)(c0 + j) * HW] = va[j] + (p.bias ? __ldg(&p.bias[c0 + j]) : 0.0f);
+        }
+        tmem_wait_ld();
+        if (c0 + 16 < Cout) {
+          if (c0 + 32 < Cout) tmem_ld16(tb + (uint32_t)(c0 + 32), va);
+          if (w < p.W) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              yb[(size_t)(c0 + 16 + j) * HW] = vb[j] + (p.bias ? __ldg(&p.bias[c0 + 16 + j]) : 0.0f);
+          }
+          tmem_wait_ld();
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&acc_empty[racc.idx]);
+      racc.next(2);
+    }
+  }
+  if (ctl && lane == 0) {
+    if (!ok || *abort_flag) {
+      // Every copy still in flight lands before the CTA can exit (the copies before the
+      // last kRowSlots were consumed, hence complete).
+      Ring back = cs.rr;
+      const uint32_t outstanding = min(cs.issued, (uint32_t)kRowSlots);
+      for (uint32_t i = 0; i < outstanding; ++i) {
+        if (back.idx == 0) {
+          back.idx = kRowSlots - 1;
+          back.phase ^= 1u;
+        } else {
+          --back.idx;
+        }
+        drain_wait(&row_full[back.idx], back.phase, p.ctl);
+      }
+    }
+    umma_commit(mma_done);
+    drain_wait(mma_done, 0, p.ctl);
+  }
+  __syncwarp();
+}
+
 template <int K>
 __global__ void __launch_bounds__(DwCfg<K>::kThreads, 1)
     dwsep_tc_kernel(const DwParams p, const __grid_constant__ CUtensorMap xmap) {
   using Cfg = DwCfg<K>;
   constexpr int P = Cfg::P;
   constexpr int kThreads = Cfg::kThreads, kDwWarps = Cfg::kDwWarps, kEpiWarp0 = Cfg::kEpiWarp0;
+  constexpr int kDwWarp0 = Cfg::kDwWarp0;
   constexpr int kWRow = Cfg::kWRow, kCMax = Cfg::kCMax;
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ uint32_t s_tmem;
@@ -207,7 +410,7 @@ __global__ void __launch_bounds__(DwCfg<K>::kThreads, 1)
     mbar_init(mma_done, 1);
     fence_mbarrier_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == Cfg::kOwnerWarp) {
     tmem_alloc(&s_tmem, kTmemCols);
     tmem_relinquish();
   }
@@ -240,7 +443,7 @@ __global__ void __launch_bounds__(DwCfg<K>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = s_tmem;
 
-  if (warp == kMmaWarp) {
+  if (!Cfg::kMerged && warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc = umma_idesc_tf32(128, Cout);
@@ -275,7 +478,7 @@ __global__ void __launch_bounds__(DwCfg<K>::kThreads, 1)
       umma_commit(mma_done);
       drain_wait(mma_done, 0, p.ctl);
     }
-  } else if (warp == kLoadWarp) {
+  } else if (!Cfg::kMerged && warp == kLoadWarp) {
     // ------------------------------------------------------------ row loader
     if (lane == 0) {
       Ring rr;
@@ -309,7 +512,7 @@ __global__ void __launch_bounds__(DwCfg<K>::kThreads, 1)
         }
       }
     }
-  } else if (warp < kEpiWarp0) {
+  } else if (warp >= kDwWarp0 && warp < kEpiWarp0) {
     // ------------------------------------------------------------ depthwise
     const int q = warp & 3;                        // TMEM lane quadrant = pixels 32q .. 32q+31
     const int grp = (warp - kDwWarp0) >> 2;        // which group of channels
@@ -383,6 +586,10 @@ __global__ void __launch_bounds__(DwCfg<K>::kThreads, 1)
       rseq += (uint32_t)(h1 - h0 + 2 * P);
     }
   dw_done:;
+  } else if (Cfg::kMerged) {
+    // ------------------------------------------------------------ epilogue + control
+    merged_epilogue<Cfg>(p, xmap, smem_b, smem_rows, row_full, row_empty, a_full, a_empty, acc_full, acc_empty,
+                         mma_done, tmem_base, abort_flag, warp, lane);
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quadrant
@@ -440,7 +647,7 @@ __global__ void __launch_bounds__(DwCfg<K>::kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == Cfg::kOwnerWarp) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
