@@ -28,18 +28,19 @@
 // of the pre-split weight block: 9 taps x [k-half 0 | k-half 1] x [hi | lo] x Cout
 // rows x 4 channels.  The ring stage is released by the MMA commit.
 //
-// Tensor memory (512 columns): two accumulator slots of T*Cout columns (units
-// alternate between them, so one unit's epilogue overlaps the next unit's MMAs), then
-// AST A stages.  An A stage holds KHG kernel rows of one (kd, K-step): T tiles x KHG x
-// 3 kw taps x [hi 8 | lo 8] columns.  Per tap and tile three MMAs (3xTF32, as in
-// conv3d_tc.cu: acc += A_hi*B_hi + A_hi*B_lo + A_lo*B_hi), N = Cout.
+// Tensor memory (512 columns): the accumulator [D_a | D_b] of 2*Cout columns, then AST
+// A stages.  An A stage holds KHG kernel rows of one (kd, K-step): KHG x 3 kw taps x
+// [hi 8 | lo 8] columns.  3xTF32 as in conv3d_tc.cu (A_hi*B_hi + A_hi*B_lo + A_lo*B_hi)
+// in two MMAs per tap: A_hi x [B_hi | B_lo] (N = 2*Cout) into [D_a | D_b] and
+// A_lo x B_hi (N = Cout) into D_a; the result is D_a + D_b.
 //
 // Roles (persistent CTAs, one per SM, 512 threads):
 //   warp 0      loader (one thread): per (unit, kd, K-step) the box and the weight block;
 //   warp 1      TMEM owner and MMA issuer (one thread);
 //   warps 4-7   A producers, one per TMEM lane quadrant: thread = position m of each tile;
-//   warps 8-15  epilogue, two teams of four taking alternate units: tcgen05.ld, + bias,
-//               activation, store (lanes = consecutive positions: coalesced rows).
+//   warps 8-15  epilogue, two teams of four, each half of the output channels: tcgen05.ld
+//               of D_a and D_b, release, + bias, activation, store (lanes = consecutive
+//               positions: coalesced rows).
 // Every wait is bounded; on a timeout all roles stop, in-flight copies and MMAs are
 // drained and TMEM is freed.
 #include <algorithm>
@@ -84,7 +85,7 @@ struct Params {
   uint32_t b_bytes;      // one weight block (9 taps): 576 * Cout
   uint32_t stage_bytes;  // x_bytes + b_bytes
   uint32_t off_bar;
-  uint32_t a_col0;       // first TMEM column of the A stages (2 * T * Cout)
+  uint32_t a_col0;       // first TMEM column of the A stages (2 * Cout: the accumulator)
   WaitCtl ctl;
 };
 
@@ -219,8 +220,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* in_empty = in_full + p.XS;        // [XS]
   uint64_t* a_full = in_empty + p.XS;         // [AST]
   uint64_t* a_empty = a_full + p.AST;         // [AST]
-  uint64_t* acc_full = a_empty + p.AST;       // [2]
-  uint64_t* acc_empty = acc_full + 2;         // [2]
+  uint64_t* acc_full = a_empty + p.AST;       // [1]
+  uint64_t* acc_empty = acc_full + 1;         // [1]
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -239,10 +240,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&a_full[i], kProdWarps);
       mbar_init(&a_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], kEpiWarps / 2);  // the four warps of the team that drained it
-    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, kEpiWarps);  // every epilogue warp, once it has read its part
     fence_mbarrier_init();
   }
   if (warp == kMmaWarp) {
@@ -300,19 +299,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = umma_idesc_tf32(128, Cout);
+      // Per tap two MMAs: A_hi x [B_hi | B_lo] (N = 2 Cout) into [D_a | D_b], then
+      // A_lo x B_hi (N = Cout) into D_a; the epilogue adds D_a + D_b.  Two instructions
+      // instead of three per tap: a single thread issues an M = 128 tf32 MMA no faster
+      // than one per ~50 cycles whatever N is up to ~96, and N = 128 runs in ~76.
+      const uint32_t idesc1 = umma_idesc_tf32(128, Cout), idesc2 = umma_idesc_tf32(128, 2 * Cout);
       const uint32_t tap_u = (uint32_t)(4 * Cout);  // one tap's block in 16-byte units: 2 halves x 2*Cout rows
-      const uint32_t lo_u = (uint32_t)Cout;         // lo rows follow the hi rows
       const uint32_t lbo = (uint32_t)(2 * Cout) * 16u;
       Ring r, ra;
       uint32_t i = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x, ++i) {
         const Unit un = decode_unit(p, u);
-        const uint32_t slot = i & 1u;
-        if (!(ok = wait_issue(&acc_empty[slot], ((i >> 1) & 1u) ^ 1u, p.ctl, abort_flag))) break;
+        if (!(ok = wait_issue(acc_empty, (i & 1u) ^ 1u, p.ctl, abort_flag))) break;
         tc_fence_after();
-        const uint32_t d0 = tmem_base + slot * (uint32_t)(T * Cout);
+        const uint32_t d0 = tmem_base;
         bool first = true;
         for (int kd = un.kd_lo; ok && kd <= un.kd_hi; ++kd) {
           for (int ks = 0; ks < p.KS; ++ks) {
@@ -329,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t a0 = tmem_base + p.a_col0 + ra.idx * (uint32_t)kAStageCols;
 #pragma unroll
               for (int tt = 0; tt < T; ++tt) {
-                const uint32_t d = d0 + (uint32_t)(tt * Cout);
+                const uint32_t d = d0 + (uint32_t)(tt * 2 * Cout);
 #pragma unroll
                 for (int khl = 0; khl < KHG; ++khl) {
 #pragma unroll
@@ -337,9 +338,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t tap = (uint32_t)((g * KHG + khl) * 3 + kw);
                     const uint32_t ac = a0 + (uint32_t)(((tt * KHG + khl) * 3 + kw) * 16);
                     const uint64_t bt = b0 + (uint64_t)(tap * tap_u);
-                    umma_tf32_ts(d, ac, bt, idesc, (first && khl == 0 && kw == 0) ? 0u : 1u);
-                    umma_tf32_ts(d, ac, bt + lo_u, idesc, 1u);
-                    umma_tf32_ts(d, ac + 8u, bt, idesc, 1u);
+                    umma_tf32_ts(d, ac, bt, idesc2, (first && khl == 0 && kw == 0) ? 0u : 1u);
+                    umma_tf32_ts(d, ac + 8u, bt, idesc1, 1u);
                   }
                 }
               }
@@ -353,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        umma_commit(&acc_full[slot]);
+        umma_commit(acc_full);
       }
       // Wait until every MMA issued above has finished reading its operands and
       // writing TMEM, whatever the path out of the loop.
@@ -418,41 +418,52 @@ __global__ void __launch_bounds__(kThreads, 1)
   producer_done:;
   } else if (warp >= kEpiWarp0) {
     // ------------------------------------------------------------ epilogue
+    // Eight warps: team t (four warps, one per TMEM lane quadrant) takes output channels
+    // [t * Cout/2, (t + 1) * Cout/2).  Each thread first reads its D_a + D_b sums into
+    // registers and releases the accumulator, then applies bias and activation and
+    // stores, so the next unit's MMAs start while the stores run.
+    constexpr int kHalfMax = kMaxCout / 2;
     const int q = warp & 3;
     const int team = (warp - kEpiWarp0) >> 2;
     const int m = q * 32 + lane;
     const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
     const int OHW = p.OH * p.OW;
+    const int half = Cout >> 1;
+    const int c0 = team * half;
     uint32_t i = 0;
     for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++i) {
-      if ((int)(i & 1u) != team) continue;
       const Unit un = decode_unit(p, u);
-      const uint32_t slot = i & 1u;
-      if (!warp_wait_relaxed(&acc_full[slot], (i >> 1) & 1u, p.ctl, abort_flag)) break;
+      if (!warp_wait_relaxed(acc_full, i & 1u, p.ctl, abort_flag)) break;
       tc_fence_after();
       // No input plane inside x: the accumulator was never written, the output is the bias.
       const bool has = un.kd_lo <= un.kd_hi;
-      float* yb = p.y + ((size_t)un.n * Cout * p.OD + un.od) * (size_t)OHW;
+      float v[kHalfMax];
 #pragma unroll
-      for (int tt = 0; tt < T; ++tt) {
-        const int pp = un.p_lo + tt * 128 + m;
-        const bool valid = pp < OHW;
-        const uint32_t taddr = lane_base + slot * (uint32_t)(T * Cout) + (uint32_t)(tt * Cout);
-        for (int cc = 0; cc < Cout; cc += 16) {
-          float v[16];
-          tmem_ld16(taddr + (uint32_t)cc, v);
+      for (int cc = 0; cc < kHalfMax; cc += 8) {
+        if (cc < half) {
+          float va[8], vb[8];
+          tmem_ld8(lane_base + (uint32_t)(c0 + cc), va);
+          tmem_ld8(lane_base + (uint32_t)(Cout + c0 + cc), vb);
           tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            float val = (has ? v[j] : 0.0f) + s_bias[cc + j];
-            if (EPI == IG3_EPI_TANH_MISH) val = tanh_mish(val);
-            if (valid) yb[(size_t)(cc + j) * p.OD * OHW + pp] = val;
-          }
+          for (int j = 0; j < 8; ++j) v[cc + j] = has ? va[j] + vb[j] : 0.0f;
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[slot]);
+      if (lane == 0) mbar_arrive(acc_empty);
+      const int pp = un.p_lo + m;
+      if (pp < OHW) {
+        float* yb = p.y + ((size_t)un.n * Cout * p.OD + un.od) * (size_t)OHW + pp;
+#pragma unroll
+        for (int cc = 0; cc < kHalfMax; ++cc) {
+          if (cc < half) {
+            float val = v[cc] + s_bias[c0 + cc];
+            if (EPI == IG3_EPI_TANH_MISH) val = tanh_mish(val);
+            yb[(size_t)(c0 + cc) * p.OD * OHW] = val;
+          }
+        }
+      }
     }
   }
   tc_fence_before();

@@ -34,7 +34,8 @@ void check(int N, int Cin, int D, int H, int W, int P, int Cout, int epi, bool v
   CHECK(p.KS * 8 >= Cin && (p.KS - 1) * 8 < Cin, "K-steps");
   // Tensor memory.
   const int a_stage_cols = T * KHG * 48;
-  CHECK(p.a_col0 == (uint32_t)(2 * T * Cout), "a_col0");
+  CHECK(T == 1 && p.a_col0 == (uint32_t)(2 * Cout), "a_col0: the accumulator [D_a | D_b]");
+  CHECK(2 * Cout <= 256, "N of the A_hi x [B_hi | B_lo] MMA");
   CHECK(p.a_col0 + (uint32_t)(p.AST * a_stage_cols) <= (uint32_t)kTmemCols, "tmem columns");
   CHECK(p.AST >= 2 && p.AST <= kMaxAST, "A stages");
   CHECK(Cout % 16 == 0 && Cout >= 16 && Cout <= 256, "MMA N");
@@ -95,8 +96,11 @@ void check(int N, int Cin, int D, int H, int W, int P, int Cout, int epi, bool v
           CHECK(s == 0, "output stored twice");
           s = 1;
         }
-        for (int cc = 0; cc < Cout; cc += 16)
-          CHECK((uint32_t)(T * Cout + tt * Cout + cc + 16) <= p.a_col0, "epilogue columns");
+        // epilogue: team t reads D_a and D_b columns of its channel half, 8 at a time
+        for (int team = 0; team < 2; ++team)
+          for (int cc = 0; cc < Cout / 2; cc += 8)
+            CHECK((uint32_t)(Cout + team * (Cout / 2) + cc + 8) <= p.a_col0 && (Cout / 2) % 8 == 0,
+                  "epilogue columns");
       }
     for (int g = 0; g < 3 / KHG; ++g)
       for (int tt = 0; tt < T; ++tt)
