@@ -109,7 +109,15 @@ static __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity,
 // batch item n, in the real input; nullptr where the position lies in the zero
 // border (or past the virtual plane).  The division by the pitch is exact for
 // pos < 2^24.
-static __device__ __forceinline__ const float* padded_src(const TcParams& p, int n, int d, int pos) {
+// What the padded convert needs of the parameters, passed by value: a reference to the
+// kernel's parameters in an out-of-line function makes the compiler copy them to local
+// memory and read every field from there inside the convert loops.
+struct PadGeom {
+  const float* x;
+  int W, pad, col0, Dr, Hr, Wr, Cin, NPOS, vec;
+};
+
+static __device__ __forceinline__ const float* padded_src(const PadGeom& p, int n, int d, int pos) {
   int h = __float2int_rz(__fdividef((float)pos, (float)p.W));
   int v = pos - h * p.W;
   if (v < 0) { --h; v += p.W; }
@@ -296,7 +304,7 @@ static __device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, floa
 // real input (padded_src) and zeros for the border.  Out of line, so that the
 // unpadded loops compile as they would without it.
 template <int KSS>
-static __device__ __noinline__ void convert_padded(const TcParams& p, int n, int d, int p0, int c0, int ct,
+static __device__ __noinline__ void convert_padded(const PadGeom p, int n, int d, int p0, int c0, int ct,
                                                    uint32_t hi_base, uint32_t lo_base) {
   constexpr int CC = KSS * 8;
   const size_t cstride = (size_t)p.Dr * p.Hr * p.Wr;
@@ -689,7 +697,8 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
             mbar_arrive(&x_empty[rx.idx]);
             rx.next((uint32_t)p.XS);
           } else if (p.pad != 0) {
-            convert_padded<KSS>(p, un.n, d, p0, c0, ct, hi_base, lo_base);
+            const PadGeom g{p.x, p.W, p.pad, p.col0, p.Dr, p.Hr, p.Wr, p.Cin, p.NPOS, p.vec};
+            convert_padded<KSS>(g, un.n, d, p0, c0, ct, hi_base, lo_base);
           } else if (p.vec) {
             // Item = (channel group, 4 consecutive positions): four 16-byte loads (one
             // per channel, coalesced along positions), transposed in registers to four
