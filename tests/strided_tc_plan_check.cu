@@ -124,7 +124,10 @@ int main() {
                      {1, 16, 6, 10, 20, 0, 16},   {1, 8, 9, 16, 16, 2, 48},  {2, 5, 5, 8, 4, 1, 16},
                      {1, 40, 6, 12, 36, 1, 128},  {1, 8, 3, 3, 4, 0, 16},    {1, 8, 4, 4, 4, 3, 16},
                      {1, 8, 5, 5, 8, 5, 16},      {3, 12, 8, 30, 60, 1, 64}, {1, 8, 4, 130, 124, 1, 16},
-                     {1, 8, 4, 6, 248, 1, 16},    {1, 17, 11, 13, 28, 2, 80}};
+                     {1, 8, 4, 6, 248, 1, 16},    {1, 17, 11, 13, 28, 2, 80}, {1, 8, 5, 6, 8, 5, 16},
+                     {1, 16, 7, 10, 24, 2, 112},  {1, 8, 5, 8, 16, 1, 96},   {1, 12, 9, 33, 36, 1, 64},
+                     {2, 24, 16, 64, 64, 1, 64},  {1, 3, 7, 9, 12, 0, 16},   {2, 8, 8, 20, 68, 1, 32},
+                     {1, 5, 5, 6, 8, 2, 48}};
   for (auto& s : shapes)
     for (int epi : {0, 1}) check(s[0], s[1], s[2], s[3], s[4], s[5], s[6], epi, epi == 1);
   srand(11);

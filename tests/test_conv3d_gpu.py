@@ -419,7 +419,7 @@ def test_conv3d_stride2_all_outputs(ig3, case, epi):
 # ---------------------------------------------------------------- stride 2 (tensor cores)
 # (N, Cin, D, H, W, Cout, pad): both A-stage shapes of the gathering kernel (three
 # kernel rows for Cout <= 112, one row for 128), ragged position tiles, Cin not a
-# multiple of 8, pad 0..3, and an output plane whose whole window lies in the padding
+# multiple of 8, pad 0..5, and an output plane whose whole window lies in the padding
 # (bias only).
 STRIDE2_TC_CASES = [
     (1, 3, 7, 9, 12, 16, 0),
@@ -430,6 +430,8 @@ STRIDE2_TC_CASES = [
     (1, 40, 6, 12, 36, 128, 1),
     (1, 8, 4, 4, 4, 16, 3),
     (2, 24, 16, 64, 64, 64, 1),
+    (1, 8, 5, 6, 8, 16, 5),       # pad 5: the staged box starts 8 columns left of x
+    (1, 16, 7, 10, 24, 112, 2),   # Cout 112: the widest three-row A stages
 ]
 
 
