@@ -16,8 +16,8 @@
 // from shared memory.  The gather is a per-lane address, so stride and padding cost
 // nothing on the tensor core.
 //
-// GEMM mapping.  M = 128 output positions p = oh*OW + ow of one output plane, T such
-// tiles per work unit (one unit = batch item, output plane od, T*128 positions);
+// GEMM mapping.  M = 128 output positions p = oh*OW + ow of one output plane (one work
+// unit = batch item, output plane od, 128 positions; the plan's T is 1);
 // N = Cout; K = Cin*27 walked as (kd, K-step of 8 channels, kh, kw).  Input planes
 // od*S + kd - P outside x are skipped (their taps read zeros).
 //
@@ -207,6 +207,7 @@ __device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, i
 template <int EPI, int T, int KHG>
 __global__ void __launch_bounds__(kThreads, 1)
     conv3d_strided_tc_kernel(const Params p, const __grid_constant__ CUtensorMap xmap) {
+  static_assert(T == 1, "the accumulator and the epilogue hold one 128-position tile per unit");
   constexpr int NG = 3 / KHG;                 // A stages per (kd, K-step)
   constexpr int kAStageCols = T * KHG * 3 * 16;
   extern __shared__ __align__(1024) uint8_t smem[];
