@@ -219,7 +219,10 @@ static __device__ __forceinline__ void issue_stage(uint32_t dcol, uint32_t tile_
 
 // All (kh, kw) taps of one A chunk against one set of accumulator columns: nine, or
 // with NKW = 1 (kw inside the MMA's N) the three kh.  Streaming weights: one ring
-// stage per tap, waited for, used and released.  Resident weights: block
+// stage per tap, waited for, used and released; the next stage's barrier is tested
+// before this stage's MMAs are issued and its result read only after them, so the
+// test's shared-memory latency (long while MMAs read their operands) overlaps the
+// issue (`next_ready` carries the result across calls).  Resident weights: block
 // (tap_base + kh * NKW + kw) * KS + blk0.  Returns false if a wait gave up (the MMAs
 // are still issued, on whatever the buffers hold; the caller stops).
 template <int T, int KSS, bool RES, bool HL, int NKW>
@@ -227,40 +230,33 @@ static __device__ __forceinline__ bool issue_taps(const TcParams& p, uint32_t dc
                                                   uint64_t ah0, uint64_t al0, uint64_t bwin, uint32_t lo_u,
                                                   uint32_t ks_u, uint32_t blk_u, uint32_t row_u, uint32_t idesc,
                                                   int tap_base, int blk0, uint64_t* b_full, uint64_t* b_empty,
-                                                  Ring& rb, volatile int* abort_flag) {
+                                                  Ring& rb, bool& next_ready, volatile int* abort_flag) {
   bool good = true;
   const uint32_t b_stage_u = blk_u * (uint32_t)KSS;
 #pragma unroll
   for (int kh = 0; kh < 3; ++kh) {
-    bool row_ready = false;
 #pragma unroll
     for (int kw = 0; kw < NKW; ++kw) {
       const uint64_t tap_u = (uint64_t)((uint32_t)kh * row_u + (uint32_t)kw);
       uint64_t bst;
+      bool ahead = false;
       if constexpr (RES) {
         bst = bwin + (uint64_t)((uint32_t)((tap_base + kh * NKW + kw) * p.KS + blk0) * blk_u);
       } else {
-        if (NKW == 3 && kw == 0) {
-          // Test the row's three stages together: with MMAs in flight each test waits
-          // behind their operand reads, and three back-to-back tests cost about one.
-          // (A stage not yet refilled reads as not ready.)
-          uint32_t i1 = rb.idx + 1, ph1 = rb.phase;
-          if (i1 == (uint32_t)p.SB) { i1 = 0; ph1 ^= 1u; }
-          uint32_t i2 = i1 + 1, ph2 = ph1;
-          if (i2 == (uint32_t)p.SB) { i2 = 0; ph2 ^= 1u; }
-          const bool r0 = mbar_test_wait(smem_addr(&b_full[rb.idx]), rb.phase);
-          const bool r1 = mbar_test_wait(smem_addr(&b_full[i1]), ph1);
-          const bool r2 = mbar_test_wait(smem_addr(&b_full[i2]), ph2);
-          row_ready = r0 && r1 && r2;
-        }
-        if (!row_ready && !wait_fast(&b_full[rb.idx], rb.phase, p.ctl, abort_flag)) good = false;
+        if (!next_ready && !wait_fast(&b_full[rb.idx], rb.phase, p.ctl, abort_flag)) good = false;
         tc_fence_after();
         bst = bwin + (uint64_t)(rb.idx * b_stage_u);
+        // The next stage's barrier, tested now and read after this stage's MMAs.  (A
+        // stage not yet refilled reads as not ready, and is then waited for.)
+        uint32_t i1 = rb.idx + 1, ph1 = rb.phase;
+        if (i1 == (uint32_t)p.SB) { i1 = 0; ph1 ^= 1u; }
+        ahead = mbar_test_wait(smem_addr(&b_full[i1]), ph1);
       }
       issue_stage<T, KSS, HL>(dcol, tile_cols, ah0 + tap_u, al0 + tap_u, bst, lo_u, ks_u, blk_u, idesc);
       if constexpr (!RES) {
         umma_commit(&b_empty[rb.idx]);
         rb.next((uint32_t)p.SB);
+        next_ready = ahead;
       }
     }
   }
@@ -544,6 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
       bool ok = true;
       if constexpr (RES) ok = wait_issue(w_full, 0, p.ctl, abort_flag);
       Ring ra, rb;
+      bool b_next_ready = false;  // the next weight stage's barrier, tested one stage ahead
       uint32_t empty_par = 0;  // per slot: uses so far, mod 2
       uint32_t plane_seq = 0;
       for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
@@ -573,12 +570,13 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
               const uint64_t bwin = b_desc0 + (uint64_t)((uint32_t)(2 - kd_hi) * slot_w);
               ok = issue_taps<T, KSS, RES, HL, (KDM == 9 ? 1 : 3)>(p, dcol, tile_cols, ah0, al0, bwin, lo_u, ks_u, blk_u,
                                                                    row_u, idesc, 0, ch * KSS, b_full, b_empty, rb,
-                                                                   abort_flag);
+                                                                   b_next_ready, abort_flag);
             } else {
               for (int kd = kd_hi; ok && kd >= kd_lo; --kd) {
                 const uint32_t dcol = tmem_base + slot_add(p, s0, d - kd - un.od0) * cout;
                 ok = issue_taps<T, KSS, RES, false, 3>(p, dcol, tile_cols, ah0, al0, b_desc0, lo_u, ks_u, blk_u, row_u,
-                                                idesc1, kd * 9, ch * KSS, b_full, b_empty, rb, abort_flag);
+                                                idesc1, kd * 9, ch * KSS, b_full, b_empty, rb, b_next_ready,
+                                                abort_flag);
                 if (ok && kd == 2 && ch == p.nchunks - 1) umma_commit(&acc_full[slot_add(p, s0, d - 2 - un.od0)]);
               }
             }
