@@ -686,7 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc16_kernel(const Params p
       const int oh = (p0 + m) / p.W;
       const int planes = un.od1 - un.od0;
       float psum = 0.0f;
-      float prev[kCout];  // the even plane's 2x2 maxima of this thread's pooled cell
+      float prev[kCout];  // the even plane of the pair: this position's scaled values
 #pragma unroll
       for (int j = 0; j < kCout; ++j) prev[j] = 0.0f;
       for (int k = 0; k < planes; ++k) {
@@ -771,12 +771,18 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc16_kernel(const Params p
               yb[(size_t)j * p.OD * OHW] = val;
             }
           }
+        } else if (od / 2 < PD && (od & 1) == 0) {
+          // The 2x2x2 max is taken d-pair first: the even plane only keeps its scaled
+          // values, so the shuffles and the exchange below run once per plane pair.
+          // (The max of a set does not depend on the order, so this is exact.)
+#pragma unroll
+          for (int j = 0; j < kCout; ++j) prev[j] = v[j] * p.inv_div;
         } else if (od / 2 < PD) {
-          // 2x2x2 max: w-pair by lane shuffle, h-pair by shuffle (W <= 16) or through
-          // shared memory (W = 32, 64), d-pair across the pair's two planes.
+          // d-pair with the even plane, w-pair by lane shuffle, h-pair by shuffle
+          // (W <= 16) or through shared memory (W = 32, 64).
 #pragma unroll
           for (int j = 0; j < kCout; ++j) {
-            const float z = v[j] * p.inv_div;
+            const float z = fmaxf(prev[j], v[j] * p.inv_div);
             v[j] = fmaxf(z, __shfl_xor_sync(0xffffffffu, z, 1));
           }
           const bool even_w = (ow & 1) == 0, even_r = (r & 1) == 0;
@@ -797,14 +803,9 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc16_kernel(const Params p
               for (int j = 0; j < kCout; ++j) v[j] = fmaxf(v[j], hb[j * 32 + cell]);
             }
           }
-          if (even_r && even_w) {
-            if ((od & 1) == 0) {
+          if (even_r && even_w && (oh >> 1) < PH && (ow >> 1) < PW) {
 #pragma unroll
-              for (int j = 0; j < kCout; ++j) prev[j] = v[j];
-            } else if ((oh >> 1) < PH && (ow >> 1) < PW) {
-#pragma unroll
-              for (int j = 0; j < kCout; ++j) psum += fmaxf(prev[j], v[j]);
-            }
+            for (int j = 0; j < kCout; ++j) psum += v[j];
           }
         }
       }
