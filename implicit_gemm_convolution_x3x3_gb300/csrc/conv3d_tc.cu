@@ -45,8 +45,9 @@
 //
 // Data flow (persistent CTAs, one per SM, 512 threads, warp-specialised):
 //   warp 0      weight producer: 1-D bulk copies (TMA) of pre-split K-step blocks from
-//               the workspace into a ring of stages (one stage = one tap's K-steps of
-//               one channel chunk), or all blocks once when they fit (resident);
+//               the workspace into a ring of stages (one stage = the K-steps of one
+//               channel chunk for two consecutive taps; KDM 9: for one kh), or all
+//               blocks once when they fit (resident);
 //   warp 1      TMEM owner and MMA issuer (one thread; descriptors are formed once
 //               and advanced by adds; the nine taps are unrolled);
 //   warps 2-7   input convert: coalesced loads of x, hi/lo split, K-major stores;
@@ -173,7 +174,8 @@ int positions_tiles(int OH, int W, int T) { return ((OH * W) + T * 128 - 1) / (T
 // Cout.  At this N an MMA is bound as much by shared-memory reads (A 4 KB + B 32 B
 // per column, at 128 B per cycle) as by its execution, and the input convert's
 // traffic (raw copy in, raw read, hi and lo out) shares the same port.
-double plane_cycles(int kdm, int hl, int nkd, int Cout, int KS, int nchunks, int T, bool res, int npos, bool xstage) {
+double plane_cycles(int kdm, int hl, int nkd, int Cout, int KS, int nchunks, int T, bool res, int tps, int npos,
+                    bool xstage) {
   if (kdm == 9) {
     const double n = 3.0 * nkd * Cout;
     const double mmas = 3.0 * KS * T * 3.0;
@@ -185,18 +187,18 @@ double plane_cycles(int kdm, int hl, int nkd, int Cout, int KS, int nchunks, int
   const int mmas_per_step = (kdm == 3) ? (hl ? 2 : 3) : 3 * nkd;
   const int n = (kdm == 3) ? nkd * Cout * (hl ? 2 : 1) : Cout;
   const double mmas = 9.0 * KS * T * mmas_per_step;
-  const double stages = res ? 0.0 : 9.0 * nchunks * (kdm == 3 ? 1 : nkd);
+  const double stages = res ? 0.0 : (double)((9 + tps - 1) / tps) * nchunks * (kdm == 3 ? 1 : nkd);
   const double mma = mmas * std::max(70.0, 0.5 * n + 5.0) + 250.0 * stages;
   const double conv = (xstage ? 0.35 : 0.9) * npos * (8.0 * KS);
   return std::max(mma, conv) + 900.0 * nchunks;  // A hand-over per chunk (mbarrier tests, commits)
 }
 
-double unit_cycles(int kdm, int hl, int planes, int Cout, int KS, int nchunks, int T, bool res, int npos,
+double unit_cycles(int kdm, int hl, int planes, int Cout, int KS, int nchunks, int T, bool res, int tps, int npos,
                    bool xstage) {
   double c = 0.0;
   for (int d = 0; d < planes + 2; ++d) {
     const int kd_hi = std::min(2, d), kd_lo = std::max(0, d - planes + 1);
-    c += plane_cycles(kdm, hl, kd_hi - kd_lo + 1, Cout, KS, nchunks, T, res, npos, xstage);
+    c += plane_cycles(kdm, hl, kd_hi - kd_lo + 1, Cout, KS, nchunks, T, res, tps, npos, xstage);
   }
   return c;
 }
@@ -235,7 +237,7 @@ Plan make_plan_uncached(int N, int Cin, int D, int H, int W, int Cout, int epi, 
   double best = 1e300;
   for (const Variant& v : kVariants) {
     if (v.kdm != kdm || v.hl != hl) continue;
-    const int T = v.t, kss = v.kss;
+    const int T = v.t, kss = v.kss, tps = v.tps;
     const bool res = v.res != 0;
     const int KS = (ks0 + kss - 1) / kss * kss;
     const int nchunks = KS / kss;
@@ -257,12 +259,13 @@ Plan make_plan_uncached(int N, int Cin, int D, int H, int W, int Cout, int epi, 
     if (res) {
       if ((long long)blob > avail) continue;
     } else {
-      sb = (int)std::min<long long>(kMaxStages, avail / ((long long)kss * blk));
-      if (sb < 3) continue;
+      sb = (int)std::min<long long>(kMaxStages, avail / ((long long)tps * kss * blk));
+      // At least two stages (one fills while the other is read) and three taps in flight.
+      if (sb < 2 || sb * tps < 3) continue;
     }
     // Raw input stages for the bulk-copy loader in what is left (at least two).
     const uint32_t x_stage = (uint32_t)(8 * kss) * npos * 4u;
-    const long long left = avail - (res ? (long long)blob : (long long)sb * kss * blk);
+    const long long left = avail - (res ? (long long)blob : (long long)sb * tps * kss * blk);
     int xs = (int)std::min<long long>(kMaxXStages, left / x_stage);
     if (xs < 2) xs = 0;
     // Planes per unit: with KDM 3 and 9 a unit's planes must fit the slots.
@@ -273,8 +276,8 @@ Plan make_plan_uncached(int N, int Cin, int D, int H, int W, int Cout, int epi, 
       const int last = OD - (S - 1) * P;
       const long long units = (long long)N * G * S;
       const int grid = (int)std::min<long long>(units, sms);
-      const double c_full = unit_cycles(kdm, hl, P, Cout, KS, nchunks, T, res, npos, xs > 0);
-      const double c_last = unit_cycles(kdm, hl, last, Cout, KS, nchunks, T, res, npos, xs > 0);
+      const double c_full = unit_cycles(kdm, hl, P, Cout, KS, nchunks, T, res, tps, npos, xs > 0);
+      const double c_last = unit_cycles(kdm, hl, last, Cout, KS, nchunks, T, res, tps, npos, xs > 0);
       // Round-robin over the grid: CTA c takes units c, c + grid, ...; a unit is
       // the last split iff u % S == S - 1.  Simulated exactly up to 65536 units; past
       // that, bounded by the rounds times the dearer unit (the difference is small
@@ -310,6 +313,7 @@ Plan make_plan_uncached(int N, int Cin, int D, int H, int W, int Cout, int epi, 
         p.units = (int)units;
         p.resident = res ? 1 : 0;
         p.SB = sb;
+        p.TPS = tps;
         p.a_half_bytes = a_half;
         p.a_stage_bytes = a_stage;
         p.b_block_bytes = blk;
@@ -317,7 +321,7 @@ Plan make_plan_uncached(int N, int Cin, int D, int H, int W, int Cout, int epi, 
         p.off_b = off_b;
         p.XS = xs;
         p.x_stage_bytes = x_stage;
-        p.off_epi = off_b + (res ? blob : (uint32_t)sb * kss * blk);
+        p.off_epi = off_b + (res ? blob : (uint32_t)(sb * tps * kss) * blk);
         p.off_x = (p.off_epi + epi_bytes + 127) / 128 * 128;
         p.off_bar = p.off_x + (uint32_t)xs * x_stage;
         pl.smem = std::max<size_t>(p.off_bar + (6 + 2 * (size_t)nslot + 2 * (size_t)sb + 2 * (size_t)xs) * 8, kMinSmem);

@@ -42,6 +42,8 @@ struct TcParams {
   int units;
   int resident;  // weights loaded once
   int SB;        // weight ring stages (streaming)
+  int TPS;       // streamed KDM 3 and 1: taps per ring stage (1, 2 or 3; with 2 the
+                 // ninth tap of a chunk sits alone in its stage); KDM 9 and resident: 1
   int XS;        // raw input stages of the bulk-copy loader (0: convert warps load x)
   int epi;
   int vec;       // convert with 16-byte loads (aligned quads of positions)
@@ -219,44 +221,53 @@ static __device__ __forceinline__ void issue_stage(uint32_t dcol, uint32_t tile_
 
 // All (kh, kw) taps of one A chunk against one set of accumulator columns: nine, or
 // with NKW = 1 (kw inside the MMA's N) the three kh.  Streaming weights: one ring
-// stage per tap, waited for, used and released; the next stage's barrier is tested
-// before this stage's MMAs are issued and its result read only after them, so the
-// test's shared-memory latency (long while MMAs read their operands) overlaps the
-// issue (`next_ready` carries the result across calls).  Resident weights: block
+// stage per TPS taps (NKW = 3) or per kh (NKW = 1, TPS = 1), waited for, used and
+// released; the next stage's barrier is tested before this stage's MMAs are issued and
+// its result read only after them, so the test's shared-memory latency (long while
+// MMAs read their operands) overlaps the issue (`next_ready` carries the result across
+// calls).  Resident weights: block
 // (tap_base + kh * NKW + kw) * KS + blk0.  Returns false if a wait gave up (the MMAs
 // are still issued, on whatever the buffers hold; the caller stops).
-template <int T, int KSS, bool RES, bool HL, int NKW>
+template <int T, int KSS, bool RES, bool HL, int NKW, int TPS>
 static __device__ __forceinline__ bool issue_taps(const TcParams& p, uint32_t dcol, uint32_t tile_cols,
                                                   uint64_t ah0, uint64_t al0, uint64_t bwin, uint32_t lo_u,
                                                   uint32_t ks_u, uint32_t blk_u, uint32_t row_u, uint32_t idesc,
                                                   int tap_base, int blk0, uint64_t* b_full, uint64_t* b_empty,
                                                   Ring& rb, bool& next_ready, volatile int* abort_flag) {
   bool good = true;
-  const uint32_t b_stage_u = blk_u * (uint32_t)KSS;
+  static_assert(TPS >= 1 && TPS <= 3 && (NKW == 3 || TPS == 1), "taps per stage");
+  const uint32_t b_tap_u = blk_u * (uint32_t)KSS;
+  uint64_t b_stage = 0;
+  bool ahead = false;
 #pragma unroll
   for (int kh = 0; kh < 3; ++kh) {
 #pragma unroll
     for (int kw = 0; kw < NKW; ++kw) {
+      const int i = kh * NKW + kw;
       const uint64_t tap_u = (uint64_t)((uint32_t)kh * row_u + (uint32_t)kw);
       uint64_t bst;
-      bool ahead = false;
       if constexpr (RES) {
-        bst = bwin + (uint64_t)((uint32_t)((tap_base + kh * NKW + kw) * p.KS + blk0) * blk_u);
+        bst = bwin + (uint64_t)((uint32_t)((tap_base + i) * p.KS + blk0) * blk_u);
       } else {
-        if (!next_ready && !wait_fast(&b_full[rb.idx], rb.phase, p.ctl, abort_flag)) good = false;
-        tc_fence_after();
-        bst = bwin + (uint64_t)(rb.idx * b_stage_u);
-        // The next stage's barrier, tested now and read after this stage's MMAs.  (A
-        // stage not yet refilled reads as not ready, and is then waited for.)
-        uint32_t i1 = rb.idx + 1, ph1 = rb.phase;
-        if (i1 == (uint32_t)p.SB) { i1 = 0; ph1 ^= 1u; }
-        ahead = mbar_test_wait(smem_addr(&b_full[i1]), ph1);
+        if (i % TPS == 0) {
+          if (!next_ready && !wait_fast(&b_full[rb.idx], rb.phase, p.ctl, abort_flag)) good = false;
+          tc_fence_after();
+          b_stage = bwin + (uint64_t)(rb.idx * (uint32_t)TPS * b_tap_u);
+          // The next stage's barrier, tested now and read after this stage's MMAs.  (A
+          // stage not yet refilled reads as not ready, and is then waited for.)
+          uint32_t i1 = rb.idx + 1, ph1 = rb.phase;
+          if (i1 == (uint32_t)p.SB) { i1 = 0; ph1 ^= 1u; }
+          ahead = mbar_test_wait(smem_addr(&b_full[i1]), ph1);
+        }
+        bst = b_stage + (uint64_t)((uint32_t)(i % TPS) * b_tap_u);
       }
       issue_stage<T, KSS, HL>(dcol, tile_cols, ah0 + tap_u, al0 + tap_u, bst, lo_u, ks_u, blk_u, idesc);
       if constexpr (!RES) {
-        umma_commit(&b_empty[rb.idx]);
-        rb.next((uint32_t)p.SB);
-        next_ready = ahead;
+        if (i % TPS == TPS - 1 || i == 3 * NKW - 1) {
+          umma_commit(&b_empty[rb.idx]);
+          rb.next((uint32_t)p.SB);
+          next_ready = ahead;
+        }
       }
     }
   }
@@ -377,8 +388,9 @@ static __device__ __noinline__ void convert_padded(const PadGeom p, int n, int d
   }
 }
 
-template <int EPI, int KDM, int T, int KSS, bool RES, bool HL>
+template <int EPI, int KDM, int T, int KSS, bool RES, bool HL, int TPS>
 __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p) {
+  static_assert((KDM == 9 || RES) ? TPS == 1 : (TPS >= 1 && TPS <= 3), "taps per weight stage");
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
@@ -478,7 +490,8 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
       } else {
         Ring rb;
         uint32_t issued = 0;
-        const uint32_t stage_bytes = (uint32_t)KSS * p.b_block_bytes;
+        const uint32_t tap_bytes = (uint32_t)KSS * p.b_block_bytes;
+        const uint32_t stage_bytes = (uint32_t)TPS * tap_bytes;
         for (int u = blockIdx.x; u < p.units && !*abort_flag; u += gridDim.x) {
           const Unit un = decode_unit(p, u);
           for (int d = un.od0; d < un.od1 + 2 && !*abort_flag; ++d) {
@@ -490,13 +503,16 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
               const int nkd = (KDM != 1) ? 1 : kd_hi - kd_lo + 1;
               for (int k = 0; k < nkd; ++k) {
                 const int tap_base = (KDM != 1) ? 0 : (kd_hi - k) * 9;
-                for (int khw = 0; khw < (KDM == 9 ? 3 : 9); ++khw) {
+                for (int khw = 0; khw < (KDM == 9 ? 3 : 9); khw += TPS) {
+                  const int nt = min(TPS, (KDM == 9 ? 3 : 9) - khw);
                   if (!wait_fast(&b_empty[rb.idx], rb.phase ^ 1u, p.ctl, abort_flag)) goto producer_done;
-                  const int blk = (tap_base + khw) * p.KS + ch * KSS;
-                  mbar_arrive_expect_tx(&b_full[rb.idx], stage_bytes);
-                  bulk_copy_g2s(smem_b + (size_t)rb.idx * stage_bytes,
-                                reinterpret_cast<const uint8_t*>(p.wblob) + (size_t)blk * p.b_block_bytes,
-                                stage_bytes, &b_full[rb.idx]);
+                  mbar_arrive_expect_tx(&b_full[rb.idx], (uint32_t)nt * tap_bytes);
+                  for (int t = 0; t < nt; ++t) {
+                    const int blk = (tap_base + khw + t) * p.KS + ch * KSS;
+                    bulk_copy_g2s(smem_b + (size_t)rb.idx * stage_bytes + (size_t)t * tap_bytes,
+                                  reinterpret_cast<const uint8_t*>(p.wblob) + (size_t)blk * p.b_block_bytes,
+                                  tap_bytes, &b_full[rb.idx]);
+                  }
                   rb.next((uint32_t)p.SB);
                   ++issued;
                 }
@@ -568,13 +584,13 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
               const uint32_t dcol = tmem_base + (s0 + (uint32_t)(d - kd_hi - un.od0)) * slot_w;
               const uint32_t idesc = umma_idesc_tf32(128, (int)(nkd * slot_w));
               const uint64_t bwin = b_desc0 + (uint64_t)((uint32_t)(2 - kd_hi) * slot_w);
-              ok = issue_taps<T, KSS, RES, HL, (KDM == 9 ? 1 : 3)>(p, dcol, tile_cols, ah0, al0, bwin, lo_u, ks_u, blk_u,
+              ok = issue_taps<T, KSS, RES, HL, (KDM == 9 ? 1 : 3), TPS>(p, dcol, tile_cols, ah0, al0, bwin, lo_u, ks_u, blk_u,
                                                                    row_u, idesc, 0, ch * KSS, b_full, b_empty, rb,
                                                                    b_next_ready, abort_flag);
             } else {
               for (int kd = kd_hi; ok && kd >= kd_lo; --kd) {
                 const uint32_t dcol = tmem_base + slot_add(p, s0, d - kd - un.od0) * cout;
-                ok = issue_taps<T, KSS, RES, false, 3>(p, dcol, tile_cols, ah0, al0, b_desc0, lo_u, ks_u, blk_u, row_u,
+                ok = issue_taps<T, KSS, RES, false, 3, TPS>(p, dcol, tile_cols, ah0, al0, b_desc0, lo_u, ks_u, blk_u, row_u,
                                                 idesc1, kd * 9, ch * KSS, b_full, b_empty, rb, b_next_ready,
                                                 abort_flag);
                 if (ok && kd == 2 && ch == p.nchunks - 1) umma_commit(&acc_full[slot_add(p, s0, d - 2 - un.od0)]);
@@ -1016,20 +1032,23 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
   }
 }
 
-// Kernel variants: (KDM, HL, T, KSS, resident).  The planner only produces these.
+// Kernel variants: (KDM, HL, T, KSS, resident, taps per weight stage).  The planner
+// only produces these.
 struct Variant {
-  int kdm, hl, t, kss, res;
+  int kdm, hl, t, kss, res, tps;
 };
 constexpr Variant kVariants[] = {
     // one MMA per split product spans the kd window (Cout 48..80)
-    {3, 0, 1, 2, 0}, {3, 0, 2, 2, 0}, {3, 0, 1, 1, 1}, {3, 0, 1, 2, 1}, {3, 0, 2, 1, 1}, {3, 0, 2, 2, 1},
+    {3, 0, 1, 2, 0, 3}, {3, 0, 2, 2, 0, 3}, {3, 0, 1, 2, 0, 2}, {3, 0, 2, 2, 0, 2}, {3, 0, 1, 2, 0, 1}, {3, 0, 2, 2, 0, 1},
+    {3, 0, 1, 1, 1, 1}, {3, 0, 1, 2, 1, 1}, {3, 0, 2, 1, 1, 1}, {3, 0, 2, 2, 1, 1},
     // hi and lo products in separate columns: two MMAs span the window (Cout 16, 32)
-    {3, 1, 1, 2, 0}, {3, 1, 2, 2, 0}, {3, 1, 1, 1, 1}, {3, 1, 1, 2, 1}, {3, 1, 2, 1, 1}, {3, 1, 2, 2, 1},
+    {3, 1, 1, 2, 0, 3}, {3, 1, 2, 2, 0, 3}, {3, 1, 1, 2, 0, 2}, {3, 1, 2, 2, 0, 2}, {3, 1, 1, 2, 0, 1}, {3, 1, 2, 2, 0, 1},
+    {3, 1, 1, 1, 1, 1}, {3, 1, 1, 2, 1, 1}, {3, 1, 2, 1, 1, 1}, {3, 1, 2, 2, 1, 1},
     // one MMA per split product spans the kd and kw window (Cout 16, W dividing 128;
     // not pool-reduce)
-    {9, 0, 1, 1, 1}, {9, 0, 1, 2, 1}, {9, 0, 2, 1, 1}, {9, 0, 2, 2, 1}, {9, 0, 1, 2, 0}, {9, 0, 2, 2, 0},
+    {9, 0, 1, 1, 1, 1}, {9, 0, 1, 2, 1, 1}, {9, 0, 2, 1, 1, 1}, {9, 0, 2, 2, 1, 1}, {9, 0, 1, 2, 0, 1}, {9, 0, 2, 2, 0, 1},
     // one MMA per kd (Cout 96..128)
-    {1, 0, 1, 2, 0}, {1, 0, 1, 1, 0},
+    {1, 0, 1, 2, 0, 3}, {1, 0, 1, 1, 0, 3}, {1, 0, 1, 2, 0, 2}, {1, 0, 1, 1, 0, 2}, {1, 0, 1, 2, 0, 1}, {1, 0, 1, 1, 0, 1},
 };
 
 // Launches the kernel variant matching p.  Returns an ig3 status.
@@ -1041,38 +1060,51 @@ int launch_kernel(const TcParams& p, size_t smem, int grid, cudaStream_t stream)
     kernel<<<grid, kThreads, smem, stream>>>(p);
     return count_launch(cuda_status(cudaGetLastError(), "conv3d TC kernel launch"));
   };
-  const int key = p.KDM * 10000 + p.HL * 1000 + p.T * 100 + p.KSS * 10 + p.resident;
+  const int key = p.KDM * 100000 + p.HL * 10000 + p.T * 1000 + p.KSS * 100 + p.resident * 10 + p.TPS;
   switch (key) {
-    case 30120: return go(conv3d_tc_kernel<EPI, 3, 1, 2, false, false>);
-    case 30220: return go(conv3d_tc_kernel<EPI, 3, 2, 2, false, false>);
-    case 30111: return go(conv3d_tc_kernel<EPI, 3, 1, 1, true, false>);
-    case 30121: return go(conv3d_tc_kernel<EPI, 3, 1, 2, true, false>);
-    case 30211: return go(conv3d_tc_kernel<EPI, 3, 2, 1, true, false>);
-    case 30221: return go(conv3d_tc_kernel<EPI, 3, 2, 2, true, false>);
-    case 31120: return go(conv3d_tc_kernel<EPI, 3, 1, 2, false, true>);
-    case 31220: return go(conv3d_tc_kernel<EPI, 3, 2, 2, false, true>);
-    case 31111: return go(conv3d_tc_kernel<EPI, 3, 1, 1, true, true>);
-    case 31121: return go(conv3d_tc_kernel<EPI, 3, 1, 2, true, true>);
-    case 31211: return go(conv3d_tc_kernel<EPI, 3, 2, 1, true, true>);
-    case 31221: return go(conv3d_tc_kernel<EPI, 3, 2, 2, true, true>);
-    case 10120: return go(conv3d_tc_kernel<EPI, 1, 1, 2, false, false>);
-    case 10110: return go(conv3d_tc_kernel<EPI, 1, 1, 1, false, false>);
+    case 301203: return go(conv3d_tc_kernel<EPI, 3, 1, 2, false, false, 3>);
+    case 302203: return go(conv3d_tc_kernel<EPI, 3, 2, 2, false, false, 3>);
+    case 301202: return go(conv3d_tc_kernel<EPI, 3, 1, 2, false, false, 2>);
+    case 302202: return go(conv3d_tc_kernel<EPI, 3, 2, 2, false, false, 2>);
+    case 301201: return go(conv3d_tc_kernel<EPI, 3, 1, 2, false, false, 1>);
+    case 302201: return go(conv3d_tc_kernel<EPI, 3, 2, 2, false, false, 1>);
+    case 301111: return go(conv3d_tc_kernel<EPI, 3, 1, 1, true, false, 1>);
+    case 301211: return go(conv3d_tc_kernel<EPI, 3, 1, 2, true, false, 1>);
+    case 302111: return go(conv3d_tc_kernel<EPI, 3, 2, 1, true, false, 1>);
+    case 302211: return go(conv3d_tc_kernel<EPI, 3, 2, 2, true, false, 1>);
+    case 311203: return go(conv3d_tc_kernel<EPI, 3, 1, 2, false, true, 3>);
+    case 312203: return go(conv3d_tc_kernel<EPI, 3, 2, 2, false, true, 3>);
+    case 311202: return go(conv3d_tc_kernel<EPI, 3, 1, 2, false, true, 2>);
+    case 312202: return go(conv3d_tc_kernel<EPI, 3, 2, 2, false, true, 2>);
+    case 311201: return go(conv3d_tc_kernel<EPI, 3, 1, 2, false, true, 1>);
+    case 312201: return go(conv3d_tc_kernel<EPI, 3, 2, 2, false, true, 1>);
+    case 311111: return go(conv3d_tc_kernel<EPI, 3, 1, 1, true, true, 1>);
+    case 311211: return go(conv3d_tc_kernel<EPI, 3, 1, 2, true, true, 1>);
+    case 312111: return go(conv3d_tc_kernel<EPI, 3, 2, 1, true, true, 1>);
+    case 312211: return go(conv3d_tc_kernel<EPI, 3, 2, 2, true, true, 1>);
+    case 101203: return go(conv3d_tc_kernel<EPI, 1, 1, 2, false, false, 3>);
+    case 101103: return go(conv3d_tc_kernel<EPI, 1, 1, 1, false, false, 3>);
+    case 101202: return go(conv3d_tc_kernel<EPI, 1, 1, 2, false, false, 2>);
+    case 101102: return go(conv3d_tc_kernel<EPI, 1, 1, 1, false, false, 2>);
+    case 101201: return go(conv3d_tc_kernel<EPI, 1, 1, 2, false, false, 1>);
+    case 101101: return go(conv3d_tc_kernel<EPI, 1, 1, 1, false, false, 1>);
     default:
       break;
   }
   if constexpr (EPI != IG3_EPI_POOL_REDUCE) {
     switch (key) {
-      case 90111: return go(conv3d_tc_kernel<EPI, 9, 1, 1, true, false>);
-      case 90121: return go(conv3d_tc_kernel<EPI, 9, 1, 2, true, false>);
-      case 90211: return go(conv3d_tc_kernel<EPI, 9, 2, 1, true, false>);
-      case 90221: return go(conv3d_tc_kernel<EPI, 9, 2, 2, true, false>);
-      case 90120: return go(conv3d_tc_kernel<EPI, 9, 1, 2, false, false>);
-      case 90220: return go(conv3d_tc_kernel<EPI, 9, 2, 2, false, false>);
+      case 901111: return go(conv3d_tc_kernel<EPI, 9, 1, 1, true, false, 1>);
+      case 901211: return go(conv3d_tc_kernel<EPI, 9, 1, 2, true, false, 1>);
+      case 902111: return go(conv3d_tc_kernel<EPI, 9, 2, 1, true, false, 1>);
+      case 902211: return go(conv3d_tc_kernel<EPI, 9, 2, 2, true, false, 1>);
+      case 901201: return go(conv3d_tc_kernel<EPI, 9, 1, 2, false, false, 1>);
+      case 902201: return go(conv3d_tc_kernel<EPI, 9, 2, 2, false, false, 1>);
       default: break;
     }
   }
-  return fail(IG3_ERR_UNSUPPORTED, "conv3d TC: no kernel variant for KDM %d, HL %d, T %d, %d K-steps, resident %d",
-              p.KDM, p.HL, p.T, p.KSS, p.resident);
+  return fail(IG3_ERR_UNSUPPORTED,
+              "conv3d TC: no kernel variant for KDM %d, HL %d, T %d, %d K-steps, resident %d, %d taps per stage", p.KDM,
+              p.HL, p.T, p.KSS, p.resident, p.TPS);
 }
 
 extern template int launch_kernel<IG3_EPI_NONE>(const TcParams&, size_t, int, cudaStream_t);

@@ -15,8 +15,8 @@ void check(int N, int Cin, int D, int H, int W, int Cout, int epi, int sms, bool
   if (flags & kNoKwWindow) CHECK(!pl.ok || pl.prm.KDM != 9, "kd x kw window in a padded plan");
   if (!pl.ok) { if (verbose) printf("NO plan %d %d %d %d %d %d epi%d: %s\n", N, Cin, D, H, W, Cout, epi, pl.why); return; }
   TcParams p = pl.prm;
-  if (verbose) printf("N%d Cin%d D%d H%d W%d Cout%d epi%d: KDM=%d HL=%d T=%d KSS=%d KS=%d nch=%d res=%d SB=%d NSLOT=%d S=%d P=%d units=%d NPOS=%d XS=%d smem=%zu\n",
-      N,Cin,D,H,W,Cout,epi,p.KDM,p.HL,p.T,p.KSS,p.KS,p.nchunks,p.resident,p.SB,p.NSLOT,p.S,p.P,p.units,p.NPOS,p.XS,pl.smem);
+  if (verbose) printf("N%d Cin%d D%d H%d W%d Cout%d epi%d: KDM=%d HL=%d T=%d KSS=%d KS=%d nch=%d res=%d SB=%d TPS=%d NSLOT=%d S=%d P=%d units=%d NPOS=%d XS=%d smem=%zu\n",
+      N,Cin,D,H,W,Cout,epi,p.KDM,p.HL,p.T,p.KSS,p.KS,p.nchunks,p.resident,p.SB,p.TPS,p.NSLOT,p.S,p.P,p.units,p.NPOS,p.XS,pl.smem);
   const int T = p.T, KSS = p.KSS;
   const uint32_t sw = (p.KDM == 9 ? 3 : p.HL ? 2 : 1) * p.Cout; const uint32_t tile_cols = p.NSLOT * sw;
   CHECK(!p.HL || p.KDM == 3, "HL needs KDM3");
@@ -32,9 +32,31 @@ void check(int N, int Cin, int D, int H, int W, int Cout, int epi, int sms, bool
   const size_t blob_need = (size_t)27 * p.KS * 64 * p.Cout * (p.HL ? 2 : 1);
   CHECK(blob_need == p.blob_bytes, "blob bytes %zu vs %u", blob_need, p.blob_bytes);
   CHECK(blob_need <= pl.blob_bytes, "blob %zu > ws %zu", blob_need, pl.blob_bytes);
-  const uint32_t stage_bytes = KSS * p.b_block_bytes;
+  const uint32_t stage_bytes = p.TPS * KSS * p.b_block_bytes;
   if (p.resident) CHECK(p.off_b + blob_need <= p.off_epi, "resident blob overlaps");
   else CHECK(p.off_b + (size_t)p.SB * stage_bytes <= p.off_epi, "ring overlaps");
+  CHECK(p.resident || (p.SB >= 2 && p.SB * p.TPS >= 3), "weight ring depth");
+  CHECK((p.KDM == 9 || p.resident) ? p.TPS == 1 : (p.TPS >= 1 && p.TPS <= 3), "taps per stage");
+  if (!p.resident) {
+    // The loader's stages (taps khw .. khw + nt - 1 copied into one stage) and the MMA
+    // issuer's (tap i read at stage offset (i % TPS) * tap bytes, the stage released
+    // after tap TPS - 1 of it or after the last tap) must agree.
+    const int ntaps = (p.KDM == 9) ? 3 : 9;
+    const uint32_t tap_bytes = KSS * p.b_block_bytes;
+    int loader_stages = 0, mma_stages = 0, copied = 0;
+    for (int khw = 0; khw < ntaps; khw += p.TPS) {
+      const int nt = std::min(p.TPS, ntaps - khw);
+      CHECK(nt * tap_bytes <= stage_bytes, "stage copy");
+      copied += nt;
+      ++loader_stages;
+    }
+    for (int i = 0; i < ntaps; ++i) {
+      CHECK((uint32_t)(i % p.TPS + 1) * tap_bytes <= stage_bytes, "tap %d beyond its stage", i);
+      if (i % p.TPS == p.TPS - 1 || i == ntaps - 1) ++mma_stages;
+    }
+    CHECK(copied == ntaps && loader_stages == mma_stages, "stages per chunk: loader %d, MMA %d", loader_stages,
+          mma_stages);
+  }
   CHECK(p.off_b >= 2 * p.a_stage_bytes, "A overlaps B");
   CHECK(p.off_bar + (6 + 2 * p.NSLOT + 2 * p.SB + 2 * p.XS) * 8 <= pl.smem, "bars beyond smem");
   CHECK(p.XS == 0 || (p.XS >= 2 && p.XS <= kMaxXStages), "xs");
@@ -138,10 +160,36 @@ int main() {
       if (s[4] % 4 == 0 && P <= 4 && s[7] != 2)
         check(s[0], s[1], s[2] + 2 * P, s[3] + 2 * P, s[4] + (P + 5) / 4 * 4, s[5], s[7], sms, sms == 152, kNoKwWindow);
     }
+  // The GPU tests' streamed-weight variant cases (tests/test_conv3d_gpu.py STAGE_CASES):
+  // each shape must still map to the variant it stands for.  {N, Cin, D, H, W, Cout, epi,
+  // KDM, HL, T, KSS, TPS}
+  int stage_cases[][12] = {
+      {1, 9, 5, 4, 280, 96, 1, 1, 0, 1, 1, 1},  {1, 9, 5, 4, 184, 96, 1, 1, 0, 1, 1, 2},
+      {1, 17, 5, 48, 8, 96, 1, 1, 0, 1, 1, 3},  {1, 17, 5, 48, 8, 96, 2, 1, 0, 1, 1, 3},
+      {8, 9, 6, 4, 288, 96, 0, 1, 0, 1, 2, 1},  {1, 9, 5, 4, 192, 128, 1, 1, 0, 1, 2, 2},
+      {1, 9, 5, 48, 8, 96, 2, 1, 0, 1, 2, 3},   {1, 9, 5, 4, 240, 48, 1, 3, 0, 1, 2, 1},
+      {1, 9, 5, 4, 168, 48, 1, 3, 0, 1, 2, 2},  {1, 9, 5, 48, 8, 80, 2, 3, 0, 1, 2, 2},
+      {1, 9, 5, 4, 152, 48, 0, 3, 0, 1, 2, 3},  {1, 9, 5, 48, 8, 64, 2, 3, 0, 1, 2, 3},
+      {4, 9, 12, 4, 200, 48, 1, 3, 0, 2, 2, 1}, {8, 9, 5, 48, 32, 80, 2, 3, 0, 2, 2, 1},
+      {4, 9, 6, 9, 168, 48, 1, 3, 0, 2, 2, 2},  {8, 9, 5, 48, 32, 64, 2, 3, 0, 2, 2, 2},
+      {4, 9, 5, 33, 96, 48, 1, 3, 0, 2, 2, 3},  {8, 9, 5, 48, 32, 48, 2, 3, 0, 2, 2, 3},
+      {1, 9, 5, 4, 288, 16, 1, 3, 1, 1, 2, 1},  {1, 9, 5, 4, 248, 16, 0, 3, 1, 1, 2, 2},
+      {1, 9, 5, 48, 8, 32, 1, 3, 1, 1, 2, 3},   {1, 9, 5, 48, 8, 32, 2, 3, 1, 1, 2, 3},
+      {4, 17, 12, 4, 224, 16, 1, 3, 1, 2, 2, 1}, {4, 17, 12, 4, 200, 16, 1, 3, 1, 2, 2, 2},
+      {8, 9, 5, 48, 32, 32, 2, 3, 1, 2, 2, 2},  {8, 17, 5, 9, 168, 16, 1, 3, 1, 2, 2, 3},
+      {1, 57, 5, 6, 128, 16, 1, 9, 0, 1, 2, 1}, {4, 57, 12, 6, 128, 16, 1, 9, 0, 2, 2, 1}};
+  for (auto& c : stage_cases) {
+    const Plan pl = make_plan(c[0], c[1], c[2], c[3], c[4], c[5], c[6], 152, 0);
+    const TcParams& p = pl.prm;
+    CHECK(pl.ok && !p.resident && p.KDM == c[7] && p.HL == c[8] && p.T == c[9] && p.KSS == c[10] && p.TPS == c[11],
+          "stage case %d %d %d %d %d %d epi%d: KDM %d HL %d T %d KSS %d res %d TPS %d", c[0], c[1], c[2], c[3], c[4],
+          c[5], c[6], p.KDM, p.HL, p.T, p.KSS, p.resident, p.TPS);
+    for (int sms : {152, 148, 7}) check(c[0], c[1], c[2], c[3], c[4], c[5], c[6], sms, false);
+  }
   // random sweep
   srand(1);
   for (int i = 0; i < 3000; ++i) {
-    int N = 1 + rand() % 4, Cin = 1 + rand() % 130, D = 3 + rand() % 40, H = 3 + rand() % 40, W = 3 + rand() % 100, Cout = 16 * (1 + rand() % 8), epi = rand() % 3;
+    int N = 1 + rand() % 4, Cin = 1 + rand() % 130, D = 3 + rand() % 40, H = 3 + rand() % 40, W = 3 + rand() % (i % 4 == 0 ? 320 : 100), Cout = 16 * (1 + rand() % 8), epi = rand() % 3;
     if (epi == 2) { int ws[] = {4, 8, 16, 32, 64}; W = ws[rand() % 5]; if (D < 4) D = 4; if (H < 4) H = 4; }
     check(N, Cin, D, H, W, Cout, epi, 1 + rand() % 160, false);
   }

@@ -182,6 +182,60 @@ def test_pool_reduce_small(ig3, shape):
             assert_close(got, ref, f"{shape} div={div} {path}")
 
 
+# One shape per streamed-weight kernel variant (KDM, HL, T, KSS, taps per weight stage),
+# each the cheapest multi-tile shape the planner maps to it; tests/planner_check.cu
+# asserts the same mapping on the CPU.  Every output against the oracle.
+STAGE_CASES = [
+    # (N, Cin, D, H, W, Cout), epilogue
+    ((1, 9, 5, 4, 280, 96), "tanh_mish"),    # KDM 1, 1 K-step chunks, 1 tap per stage
+    ((1, 9, 5, 4, 184, 96), "tanh_mish"),    # KDM 1, 1 K-step chunks, 2 taps
+    ((1, 17, 5, 48, 8, 96), "tanh_mish"),    # KDM 1, 1 K-step chunks, 3 taps
+    ((1, 17, 5, 48, 8, 96), "pool_reduce"),
+    ((8, 9, 6, 4, 288, 96), "none"),         # KDM 1, 2 K-step chunks, 1 tap
+    ((1, 9, 5, 4, 192, 128), "tanh_mish"),   # KDM 1, 2 K-step chunks, 2 taps
+    ((1, 9, 5, 48, 8, 96), "pool_reduce"),   # KDM 1, 2 K-step chunks, 3 taps
+    ((1, 9, 5, 4, 240, 48), "tanh_mish"),    # KDM 3, one tile, 1 tap
+    ((1, 9, 5, 4, 168, 48), "tanh_mish"),    # KDM 3, one tile, 2 taps
+    ((1, 9, 5, 48, 8, 80), "pool_reduce"),
+    ((1, 9, 5, 4, 152, 48), "none"),         # KDM 3, one tile, 3 taps
+    ((1, 9, 5, 48, 8, 64), "pool_reduce"),
+    ((4, 9, 12, 4, 200, 48), "tanh_mish"),   # KDM 3, two tiles, 1 tap
+    ((8, 9, 5, 48, 32, 80), "pool_reduce"),
+    ((4, 9, 6, 9, 168, 48), "tanh_mish"),    # KDM 3, two tiles, 2 taps
+    ((8, 9, 5, 48, 32, 64), "pool_reduce"),
+    ((4, 9, 5, 33, 96, 48), "tanh_mish"),    # KDM 3, two tiles, 3 taps
+    ((8, 9, 5, 48, 32, 48), "pool_reduce"),
+    ((1, 9, 5, 4, 288, 16), "tanh_mish"),    # KDM 3 hi/lo columns, one tile, 1 tap
+    ((1, 9, 5, 4, 248, 16), "none"),         # KDM 3 hi/lo columns, one tile, 2 taps
+    ((1, 9, 5, 48, 8, 32), "tanh_mish"),     # KDM 3 hi/lo columns, one tile, 3 taps
+    ((1, 9, 5, 48, 8, 32), "pool_reduce"),
+    ((4, 17, 12, 4, 224, 16), "tanh_mish"),  # KDM 3 hi/lo columns, two tiles, 1 tap
+    ((4, 17, 12, 4, 200, 16), "tanh_mish"),  # KDM 3 hi/lo columns, two tiles, 2 taps
+    ((8, 9, 5, 48, 32, 32), "pool_reduce"),
+    ((8, 17, 5, 9, 168, 16), "tanh_mish"),   # KDM 3 hi/lo columns, two tiles, 3 taps
+    ((1, 57, 5, 6, 128, 16), "tanh_mish"),   # KDM 9 (kd x kw window), one tile, streamed
+    ((4, 57, 12, 6, 128, 16), "tanh_mish"),  # KDM 9, two tiles, streamed
+]
+
+
+@pytest.mark.parametrize("case", STAGE_CASES, ids=lambda c: "x".join(map(str, c[0])) + "-" + c[1])
+def test_conv3d_weight_stage_variants_all_outputs(ig3, case):
+    shape, epi = case
+    N, Cin, D, H, W, Cout = shape
+    assert tc_supported(ig3, N, Cin, D, H, W, Cout, epi)
+    wl = si.conv3d_workload("t", N, Cin, D, H, W, Cout, seed=3000 + sum(shape), epilogue=epi,
+                            bias2=(epi == "pool_reduce"))
+    t = wl.generate_all()
+    if epi == "pool_reduce":
+        ref = oracle.conv3d_pool_reduce(t["x"], t["w"], t["b"], 2.0, 2, t["bias2"])
+        got = run_conv(ig3, t, epi, "tc", params={"divisor": 2.0, "pool": 2})
+    else:
+        y = oracle.conv3d(t["x"], t["w"], t["b"])
+        ref = oracle.tanh_mish(y) if epi == "tanh_mish" else y
+        got = run_conv(ig3, t, epi, "tc")
+    assert_close(got, ref, f"{shape} {epi}")
+
+
 def test_pool_reduce_full_size_sampled_and_deterministic(ig3):
     wl = si.conv3d_pool_reduce()
     t = wl.generate_all()
