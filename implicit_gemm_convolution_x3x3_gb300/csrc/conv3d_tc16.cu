@@ -263,6 +263,19 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// The 16 channels of one output position: + activation, stored (NCDHW, 16 channels).
+template <int EPI>
+__device__ __forceinline__ void store_position(const Params& p, int n, int od, int oh, int ow, const float (&v)[kCout]) {
+  const size_t OHW = (size_t)p.OH * p.OW;
+  float* yb = p.y + ((size_t)n * kCout * p.OD + od) * OHW + (size_t)oh * p.OW + ow;
+#pragma unroll
+  for (int j = 0; j < kCout; ++j) {
+    float val = v[j];
+    if (EPI == IG3_EPI_TANH_MISH) val = tanh_mish(val);
+    yb[(size_t)j * p.OD * OHW] = val;
+  }
+}
+
 // bar.sync that also returns the AND of v over the participating threads.
 __device__ __forceinline__ bool named_bar_and(int id, int count, bool v) {
   uint32_t r;
@@ -401,10 +414,13 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc16_kernel(const Params p
   __shared__ int s_abort;
   __shared__ float s_red[kEpiWarps];
   __shared__ __align__(16) float s_bias[kCout];
-  // kw hand-over across quadrants: [team][buffer][quadrant][48]
-  __shared__ float s_kx[2][2][4][48];
-  // h-pair hand-over of the pooled maxima: [team][buffer][channel][cell]
-  __shared__ float s_h[2][2][kCout][32];
+  // kw hand-over across quadrants: [team][buffer][quadrant][lane 0: block 1, block 2 |
+  // lane 1: block 2] x 16 channels
+  __shared__ __align__(16) float s_kx[2][2][4][48];
+  // h-pair hand-over of the pooled maxima: [team][buffer][cell][16 channels], the four
+  // 16-byte granules of a cell rotated by (cell >> 1) & 3 so that the 16 cells a warp
+  // writes or reads at once spread over all banks
+  __shared__ __align__(16) float s_h[2][2][32][kCout];
 
   uint8_t* smem_b = smem;
   uint8_t* smem_x = smem + p.off_x;
@@ -731,15 +747,14 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc16_kernel(const Params p
           // two wrap-around columns).  Two buffers alternate, one barrier per plane.
           kx_buf ^= 1u;
           if (q > 0 && lane < 2) {
+            float4* d = reinterpret_cast<float4*>(xb + q * 48);
+            if (lane == 0) {
 #pragma unroll
-            for (int j = 0; j < kCout; ++j) {
-              if (lane == 0) {
-                xb[q * 48 + j] = a1[j];
-                xb[q * 48 + 16 + j] = a2[j];
-              } else {
-                xb[q * 48 + 32 + j] = a2[j];
-              }
+              for (int i = 0; i < 4; ++i) d[i] = make_float4(a1[4 * i], a1[4 * i + 1], a1[4 * i + 2], a1[4 * i + 3]);
             }
+            d += (lane == 0) ? 4 : 8;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) d[i] = make_float4(a2[4 * i], a2[4 * i + 1], a2[4 * i + 2], a2[4 * i + 3]);
           }
           named_bar_sync(4 + team, 128);
         }
@@ -749,13 +764,20 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc16_kernel(const Params p
           a2[j] = __shfl_down_sync(0xffffffffu, a2[j], 2);
         }
         if (p.W > 32 && q < 3 && lane >= 30) {
+          // Lane 31 takes blocks 1 and 2 of the next quadrant's lane 0 and 1, lane 30
+          // block 2 of its lane 0.
+          const float4* src = reinterpret_cast<const float4*>(xb + (q + 1) * 48);
+          const float4* s2 = src + ((lane == 31) ? 8 : 4);
 #pragma unroll
-          for (int j = 0; j < kCout; ++j) {
-            if (lane == 31) {
-              a1[j] = xb[(q + 1) * 48 + j];
-              a2[j] = xb[(q + 1) * 48 + 32 + j];
-            } else {
-              a2[j] = xb[(q + 1) * 48 + 16 + j];
+          for (int i = 0; i < 4; ++i) {
+            const float4 t = s2[i];
+            a2[4 * i] = t.x; a2[4 * i + 1] = t.y; a2[4 * i + 2] = t.z; a2[4 * i + 3] = t.w;
+          }
+          if (lane == 31) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float4 t = src[i];
+              a1[4 * i] = t.x; a1[4 * i + 1] = t.y; a1[4 * i + 2] = t.z; a1[4 * i + 3] = t.w;
             }
           }
         }
@@ -763,13 +785,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc16_kernel(const Params p
         for (int j = 0; j < kCout; ++j) v[j] += a1[j] + a2[j];
         if constexpr (EPI != IG3_EPI_POOL_REDUCE) {
           if (oh < p.OH && ow < p.OW) {
-            float* yb = p.y + ((size_t)un.n * kCout * p.OD + od) * OHW + (size_t)oh * p.OW + ow;
-#pragma unroll
-            for (int j = 0; j < kCout; ++j) {
-              float val = v[j];
-              if (EPI == IG3_EPI_TANH_MISH) val = tanh_mish(val);
-              yb[(size_t)j * p.OD * OHW] = val;
-            }
+            store_position<EPI>(p, un.n, od, oh, ow, v);
           }
         } else if (od / 2 < PD && (od & 1) == 0) {
           // The 2x2x2 max is taken d-pair first: the even plane only keeps its scaled
@@ -791,16 +807,24 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc16_kernel(const Params p
 #pragma unroll
             for (int j = 0; j < kCout; ++j) v[j] = fmaxf(v[j], __shfl_xor_sync(0xffffffffu, v[j], p.W));
           } else {
-            float* hb = &s_h[team][h_buf][0][0];
+            float4* hc = reinterpret_cast<float4*>(&s_h[team][h_buf][cell][0]);
+            const int rot = (cell >> 1) & 3;
             h_buf ^= 1u;
             if (!even_r && even_w) {
 #pragma unroll
-              for (int j = 0; j < kCout; ++j) hb[j * 32 + cell] = v[j];
+              for (int i = 0; i < 4; ++i)
+                hc[i ^ rot] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
             }
             named_bar_sync(1 + team, 128);
             if (even_r && even_w) {
 #pragma unroll
-              for (int j = 0; j < kCout; ++j) v[j] = fmaxf(v[j], hb[j * 32 + cell]);
+              for (int i = 0; i < 4; ++i) {
+                const float4 t = hc[i ^ rot];
+                v[4 * i] = fmaxf(v[4 * i], t.x);
+                v[4 * i + 1] = fmaxf(v[4 * i + 1], t.y);
+                v[4 * i + 2] = fmaxf(v[4 * i + 2], t.z);
+                v[4 * i + 3] = fmaxf(v[4 * i + 3], t.w);
+              }
             }
           }
           if (even_r && even_w && (oh >> 1) < PH && (ow >> 1) < PW) {
