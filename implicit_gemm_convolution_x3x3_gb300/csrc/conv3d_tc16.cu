@@ -437,7 +437,6 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc16_kernel(const Params p
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   volatile int* abort_flag = &s_abort;
-  const int HW = p.H * p.W;
 
   if (tid < kCout) s_bias[tid] = p.bias ? p.bias[tid] : 0.0f;
   if (tid == 0) {
@@ -687,7 +686,6 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc16_kernel(const Params p
     const int m = q * 32 + lane;
     const int et = tid - kEpiWarp0 * 32;
     const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
-    const size_t OHW = (size_t)p.OH * p.OW;
     const int PH = p.OH / 2, PW = p.OW / 2, PD = p.OD / 2;
     const uint32_t nslot = (uint32_t)p.NSLOT;
     // Tiles hold whole rows, so a lane has the same column in every tile.
@@ -948,6 +946,7 @@ Plan make_plan_uncached(int N, int Cin, int D, int H, int W, int Cout, int epi, 
   double best = 1e300;
   for (const auto& shape : kShapes) {
     const int kss = shape[0], pp = shape[1], ast = shape[2];
+    if (ast > kMaxAStages) continue;
     if (kss == 2 && ks0 == 1) continue;
     const int KS = (ks0 + kss - 1) / kss * kss;
     const int nchunks = KS / kss;
