@@ -269,10 +269,11 @@ __device__ __forceinline__ void store_position(const Params& p, int n, int od, i
   const size_t OHW = (size_t)p.OH * p.OW;
   float* yb = p.y + ((size_t)n * kCout * p.OD + od) * OHW + (size_t)oh * p.OW + ow;
 #pragma unroll
-  for (int j = 0; j < kCout; ++j) {
-    float val = v[j];
-    if (EPI == IG3_EPI_TANH_MISH) val = tanh_mish(val);
-    yb[(size_t)j * p.OD * OHW] = val;
+  for (int j = 0; j < kCout; j += 2) {
+    float v0 = v[j], v1 = v[j + 1];
+    if (EPI == IG3_EPI_TANH_MISH) tanh_mish2(v0, v1, v0, v1);
+    yb[(size_t)j * p.OD * OHW] = v0;
+    yb[(size_t)(j + 1) * p.OD * OHW] = v1;
   }
 }
 

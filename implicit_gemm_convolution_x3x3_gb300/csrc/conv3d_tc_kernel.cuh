@@ -919,10 +919,11 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
             if (oh < p.OH && ow >= 0 && ow < p.OW) {
               float* yb = p.y + (((size_t)un.n * p.Cout + c0) * p.OD + od) * OHW + (size_t)oh * p.OW + ow;
 #pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                float val = v[t][j];
-                if (EPI == IG3_EPI_TANH_MISH) val = tanh_mish(val);
-                yb[(size_t)j * p.OD * OHW] = val;
+              for (int j = 0; j < 8; j += 2) {
+                float v0 = v[t][j], v1 = v[t][j + 1];
+                if (EPI == IG3_EPI_TANH_MISH) tanh_mish2(v0, v1, v0, v1);
+                yb[(size_t)j * p.OD * OHW] = v0;
+                yb[(size_t)(j + 1) * p.OD * OHW] = v1;
               }
             }
           }
@@ -957,10 +958,13 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc_kernel(const TcParams p
           if constexpr (EPI != IG3_EPI_POOL_REDUCE) {
             float* yb = p.y + (((size_t)un.n * p.Cout + c0) * p.OD + od) * OHW + (size_t)oh * p.OW + ow;
 #pragma unroll
-            for (int j = 0; j < CW; ++j) {
-              float val = v[j];
-              if (EPI == IG3_EPI_TANH_MISH) val = tanh_mish(val);
-              if (valid) yb[(size_t)j * p.OD * OHW] = val;
+            for (int j = 0; j < CW; j += 2) {
+              float v0 = v[j], v1 = v[j + 1];
+              if (EPI == IG3_EPI_TANH_MISH) tanh_mish2(v0, v1, v0, v1);
+              if (valid) {
+                yb[(size_t)j * p.OD * OHW] = v0;
+                yb[(size_t)(j + 1) * p.OD * OHW] = v1;
+              }
             }
           } else {
             if (!pool_plane) continue;

@@ -280,4 +280,63 @@ __device__ __forceinline__ float tanh_mish(float y) {
   return tanh_from_exp(y * __fdividef(t, t + 2.0f));
 }
 
+// Two fp32 values in one 64-bit register, for the packed two-lane instructions
+// (add / mul / fma .rn.f32x2: each lane rounded as its scalar instruction would be).
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+// 2^x and 1/x from the approximate special-function instructions, on both lanes.
+__device__ __forceinline__ uint64_t f2_ex2(uint64_t v) {
+  float a, b;
+  f2_unpack(v, a, b);
+  asm("ex2.approx.ftz.f32 %0, %0;" : "+f"(a));
+  asm("ex2.approx.ftz.f32 %0, %0;" : "+f"(b));
+  return f2_pack(a, b);
+}
+__device__ __forceinline__ uint64_t f2_rcp(uint64_t v) {
+  float a, b;
+  f2_unpack(v, a, b);
+  asm("rcp.approx.ftz.f32 %0, %0;" : "+f"(a));
+  asm("rcp.approx.ftz.f32 %0, %0;" : "+f"(b));
+  return f2_pack(a, b);
+}
+
+// tanh(mish(y)) of two values, the same formula as tanh_mish with the exponentials
+// written as powers of two (e^x = 2^(x log2 e)): n = 2^(min(y,15) log2 e),
+// t = n(n+2), mish = y t / (t+2), and tanh(mish) = 1 - 2 / (2^(2 log2 e * mish) + 1).
+// The arithmetic between the special-function instructions runs on the packed
+// two-lane instructions, about 9.5 instructions per value instead of 15.
+__device__ __forceinline__ void tanh_mish2(float y0, float y1, float& o0, float& o1) {
+  constexpr float kLog2e = 1.44269504088896340736f;
+  const uint64_t y = f2_pack(y0, y1);
+  const uint64_t n = f2_ex2(f2_mul(f2_pack(fminf(y0, 15.0f), fminf(y1, 15.0f)), f2_pack(kLog2e, kLog2e)));
+  const uint64_t two = f2_pack(2.0f, 2.0f);
+  const uint64_t t = f2_mul(n, f2_add(n, two));
+  const uint64_t tr = f2_mul(t, f2_rcp(f2_add(t, two)));  // t / (t + 2)
+  const uint64_t b = f2_mul(f2_mul(y, f2_pack(2.0f * kLog2e, 2.0f * kLog2e)), tr);
+  const uint64_t one = f2_pack(1.0f, 1.0f);
+  const uint64_t s = f2_rcp(f2_add(f2_ex2(b), one));
+  f2_unpack(f2_fma(s, f2_pack(-2.0f, -2.0f), one), o0, o1);
+}
+
 }  // namespace ig3

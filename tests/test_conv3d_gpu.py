@@ -111,16 +111,18 @@ def test_conv3d_without_bias(ig3):
         assert_close(run_conv(ig3, t, "tanh_mish", path), ref, f"no bias {path}")
 
 
-def test_activation_over_wide_range(ig3):
+@pytest.mark.parametrize("shape", [(1, 8, 4, 6, 64, 16), (1, 8, 4, 6, 64, 64), (1, 8, 4, 6, 128, 16)],
+                         ids=["cout16_a_in_tmem", "cout64_kd_window", "cout16_kd_kw_window"])
+def test_activation_over_wide_range(ig3, shape):
     # Large weights drive conv outputs across [-60, 60]: exercises both branches
-    # of the activation and its saturation.
-    wl = si.conv3d_workload("t", 1, 8, 4, 6, 64, 16, seed=78, epilogue="tanh_mish", wb_bound=2.5,
+    # of the activation and its saturation, in each tensor-core epilogue.
+    wl = si.conv3d_workload("t", *shape, seed=78, epilogue="tanh_mish", wb_bound=2.5,
                             x_dist=("uniform", -3.0, 3.0))
     t = wl.generate_all()
     y = oracle.conv3d(t["x"], t["w"], t["b"])
     assert y.min() < -20 and y.max() > 20
     ref = oracle.tanh_mish(y)
-    for path in paths_for(ig3, (1, 8, 4, 6, 64, 16), "tanh_mish"):
+    for path in paths_for(ig3, shape, "tanh_mish"):
         assert_close(run_conv(ig3, t, "tanh_mish", path), ref, f"wide range {path}")
 
 
