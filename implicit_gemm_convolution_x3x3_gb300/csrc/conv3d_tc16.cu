@@ -489,6 +489,11 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc16_kernel(const Params p
   if (warp == kLoadWarp) {
     // ------------------------------------------------------------ loader
     if (lane == 0) {
+      // The weight blocks come from the split kernel launched just before this one;
+      // with a programmatic dependent launch this CTA may already run beside it, so
+      // wait for that grid's completion (and its writes) here.  Without one it is a
+      // no-op.
+      asm volatile("griddepcontrol.wait;" ::: "memory");
       mbar_arrive_expect_tx(w_full, p.blob_bytes);
       const uint8_t* wsrc = reinterpret_cast<const uint8_t*>(p.wblob);
       for (uint32_t off = 0; off < p.blob_bytes;) {
@@ -865,6 +870,9 @@ __global__ void __launch_bounds__(kThreads, 1) conv3d_tc16_kernel(const Params p
 // x 16 channels; channel ks*8 + khalf*4 + j of the row, zero past Cin.
 __global__ void tc16_prep_weights(const float* __restrict__ w, float* __restrict__ blob, int Cin, int KS,
                                   int total) {
+  // The conv kernel that follows may start now (programmatic dependent launch): only
+  // its copy of these blocks waits for this grid to finish.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
     const int j = i & 3;
     int t = i >> 2;
@@ -1036,8 +1044,19 @@ int launch(const Params& p, const CUtensorMap& xmap, size_t smem, int grid, cuda
   auto kernel = conv3d_tc16_kernel<EPI, KSS, PP>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return cuda_status(e, "conv3d TC16: set shared memory size");
-  kernel<<<grid, kThreads, smem, stream>>>(p, xmap);
-  return count_launch(cuda_status(cudaGetLastError(), "conv3d TC16 kernel launch"));
+  // Programmatic dependent launch: the kernel's set-up overlaps the weight split.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kernel, p, xmap);
+  return count_launch(cuda_status(e, "conv3d TC16 kernel launch"));
 }
 
 template <int EPI>
